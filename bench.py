@@ -1,0 +1,421 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA hot path on one GB300 (or N replicas under torchrun).
+
+One step = one pass of the whole path over one batch of synthetic input:
+  * chunk prefill of the varlen workload (8 sequences, lengths U[512, 4096], H = 32, d = 128,
+    bf16 q/k/v, fp32 gates, chunk 64, states from a 512-slot fp32 pool)       -> headline value
+  * single-token decode (256 requests, H = 32, d = 128, pool updated in place) -> "decode"
+  * scalar-gate verify (64 requests x 4 drafts, intermediate states written)  -> "verify"
+Every input lives in HBM before the timed region; each of the three working sets is larger than
+the 129 MB L2, so no L2 flush is needed between steps.  Kernel durations come from CUDA events
+recorded on the launching stream (the prefill's three kernels through kda_chunk_prefill_timed).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle instead, on a
+bounded sample of the prefill workload, and prints the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill tokens/s and decode tokens/s (state GB/s, % HBM/tensor roofline)"
+UNIT = "tokens/s"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------------------------------------
+# algorithmic bytes (mandatory traffic: inputs once, outputs once, each state read + written once)
+# ---------------------------------------------------------------------------------------------
+def prefill_bytes(T, N_active, H, D, io_bytes, out_bytes):
+    per_token_head = 3 * D * io_bytes + D * 4 + 4 + D * out_bytes      # q,k,v + g_raw + b_raw + out
+    state = 2 * D * D * 4                                               # read + write per (seq, head)
+    params = H * 4 + H * D * 4                                          # A_log, dt_bias
+    return T * H * per_token_head + N_active * H * state + params
+
+
+def decode_bytes(B, H, D, io_bytes, out_bytes):
+    return B * H * (2 * D * D * 4 + 3 * D * io_bytes + D * 4 + 4 + D * out_bytes) + H * 4 + H * D * 4
+
+
+def verify_bytes(B, Td, H, D, io_bytes, out_bytes, per_head_gate=True):
+    g = 4 if per_head_gate else D * 4
+    per_token = D * D * 4 + 3 * D * io_bytes + g + 4 + D * out_bytes    # inter-state write + inputs + out
+    return B * H * (D * D * 4 + Td * per_token) + H * 8
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        self.file.flush()
+        self.file.seek(0)
+        rows = [l.strip().split(", ") for l in self.file.read().splitlines() if l.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            if len(r) < 10:
+                continue
+            try:
+                sm.append(float(r[2]))
+                smax.append(float(r[3]))
+                power.append(float(r[4]))
+            except ValueError:
+                continue
+            for n, val in zip(names, r[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(n)
+        # samples under load: the top half by SM clock / power are the timed region's
+        loaded = [s for s, p in zip(sm, power) if p >= statistics.median(power)] if power else sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------------------------
+# distributed helpers (replicas; the path has no exchange step)
+# ---------------------------------------------------------------------------------------------
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def maybe_init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def reduce_max(dist, x, device):
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU oracle timing (baseline and reference arm)
+# ---------------------------------------------------------------------------------------------
+_PREFILL_HOST = {}
+
+
+def oracle_prefill_sample(n_tokens):
+    """Oracle prefill of the first ``n_tokens`` tokens of the varlen workload's first sequence, all
+    32 heads, threads over heads.  Returns (seconds, threads)."""
+    import torch
+    import oracle
+    from kda_gated_delta_gb300 import workloads
+
+    if "inp" not in _PREFILL_HOST:
+        _PREFILL_HOST["inp"] = workloads.workload_inputs(1)
+    inp = _PREFILL_HOST["inp"]
+    n = int(n_tokens)
+    sub = {k: inp[k][:n] for k in ("q", "k", "v", "g_raw", "b_raw")}
+    cu = torch.tensor([0, n], dtype=torch.int32)
+    sidx = inp["state_idx"][:1]
+    pool = inp["pool"][sidx.long()]
+    threads = min(len(os.sched_getaffinity(0)), 32)
+    p = oracle.make_params(32, 128)
+    t0 = time.perf_counter()
+    oracle.forward(p, sub["q"], sub["k"], sub["v"], sub["g_raw"], sub["b_raw"], inp["A_log"], inp["dt_bias"],
+                   cu, pool, torch.zeros(1, dtype=torch.int32), nthreads=threads)
+    return time.perf_counter() - t0, threads
+
+
+def cpu_baseline(target_s=12.0):
+    """Time the oracle as it stands on a bounded sample (about target_s seconds of CPU work)."""
+    t, thr = oracle_prefill_sample(32)
+    n = int(max(32, min(4096, 32 * target_s / max(t, 1e-3))))
+    t, thr = oracle_prefill_sample(n)
+    return {"value": n / t, "unit": UNIT, "cores": thr, "kind": "oracle",
+            "sample": f"fp64 token recurrence over the first {n} tokens of the varlen workload's first "
+                      f"sequence, all 32 heads (threads over heads), {t:.1f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    n = 128
+    for _ in range(args.warmup):
+        oracle_prefill_sample(n)
+    times, thr = [], 1
+    for _ in range(args.steps):
+        t, thr = oracle_prefill_sample(n)
+        times.append(t)
+    total = sum(times)
+    value = n * args.steps / total
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": "varlen_prefill_bf16 (sampled: first 128 tokens of sequence 0, 32 heads)",
+                       "num_heads": 32, "head_dim": 128, "chunk_size": 64},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
+                             "sample": f"{n} tokens x 32 heads per step, fp64 token recurrence"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    dist = maybe_init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from kda_gated_delta_gb300 import build as kbuild
+    kbuild.build()
+    import kda_gated_delta_gb300 as kda
+    from kda_gated_delta_gb300 import workloads
+
+    bw_peak, _, peak_src = peaks()
+    H, D = 32, 128
+
+    # ---- inputs, resident in HBM --------------------------------------------------------------
+    wp, wd, wv = workloads.workload(1), workloads.workload(2), workloads.workload(4)
+    pre_h = workloads.workload_inputs(1)
+    dec_h = workloads.workload_inputs(2)
+    ver_h = workloads.workload_inputs(4)
+    pre, dec, ver = (workloads.to_device(x, dev) for x in (pre_h, dec_h, ver_h))
+    T = int(pre_h["cu_seqlens"][-1])
+    Np = len(wp.lengths)
+    p_pre = kda.make_params(H, D, io_dtype=torch.bfloat16, out_dtype=torch.bfloat16, chunk_size=64)
+    p_dec = kda.make_params(H, D, io_dtype=torch.bfloat16, out_dtype=torch.bfloat16)
+    p_ver = kda.make_params(H, D, io_dtype=torch.bfloat16, out_dtype=torch.bfloat16, gate="gdn")
+    ws = torch.empty(kda.prefill_workspace_size(p_pre, Np, T), dtype=torch.uint8, device=dev)
+    out_pre = torch.empty(T, H, D, dtype=torch.bfloat16, device=dev)
+    out_dec = torch.empty(wd.batch, H, D, dtype=torch.bfloat16, device=dev)
+    out_ver = torch.empty(wv.batch * wv.t_draft, H, D, dtype=torch.bfloat16, device=dev)
+    inter = torch.empty(wv.batch, wv.t_draft, H, D, D, dtype=torch.float32, device=dev)
+
+    K, W = args.steps, args.warmup
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    pre_ev = [[ev() for _ in range(4)] for _ in range(K + W)]
+    dec_ev = [[ev(), ev()] for _ in range(K + W)]
+    ver_ev = [[ev(), ev()] for _ in range(K + W)]
+    for e in [x for row in pre_ev for x in row]:
+        e.record()          # create the underlying CUDA events before handing them to the library
+    torch.cuda.synchronize()
+    launches_per_step = 3 + 1 + 1
+
+    def step(i):
+        kda.chunk_prefill(pre["q"], pre["k"], pre["v"], pre["g_raw"], pre["b_raw"], pre["A_log"],
+                          pre["dt_bias"], pre["cu_seqlens"], pre["pool"], pre["state_idx"], out_pre,
+                          params=p_pre, workspace=ws, events=pre_ev[i])
+        dec_ev[i][0].record()
+        kda.recurrent_decode(dec["q"], dec["k"], dec["v"], dec["g_raw"], dec["b_raw"], dec["A_log"],
+                             dec["dt_bias"], dec["pool"], dec["state_idx"], out_dec, params=p_dec)
+        dec_ev[i][1].record()
+        ver_ev[i][0].record()
+        kda.recurrent_verify(ver["q"], ver["k"], ver["v"], ver["g_raw"], ver["b_raw"], ver["A_log"],
+                             ver["dt_bias"], ver["pool"], ver["state_idx"], wv.t_draft, inter, out_ver,
+                             params=p_ver)
+        ver_ev[i][1].record()
+
+    for i in range(W):
+        step(K + i)
+    torch.cuda.synchronize()
+    if kda.check_device_errors() != 0:
+        raise RuntimeError("device error recorded during warm-up")
+
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(dist)
+    torch.cuda.synchronize()
+    t_start, t_end = ev(), ev()
+    t_start.record()
+    for i in range(K):
+        step(i)
+    t_end.record()
+    torch.cuda.synchronize()
+    barrier(dist)
+    clk = clocks.stop()
+
+    step_ms = reduce_max(dist, t_start.elapsed_time(t_end) / K, dev)
+    ph = [[pre_ev[i][j].elapsed_time(pre_ev[i][j + 1]) for j in range(3)] for i in range(K)]
+    phase_ms = [sum(r[j] for r in ph) / K for j in range(3)]
+    pre_ms = reduce_max(dist, sum(phase_ms), dev)
+    dec_ms = reduce_max(dist, sum(dec_ev[i][0].elapsed_time(dec_ev[i][1]) for i in range(K)) / K, dev)
+    ver_ms = reduce_max(dist, sum(ver_ev[i][0].elapsed_time(ver_ev[i][1]) for i in range(K)) / K, dev)
+
+    pre_B = prefill_bytes(T, Np, H, D, 2, 2)
+    dec_B = decode_bytes(wd.batch, H, D, 2, 2)
+    ver_B = verify_bytes(wv.batch, wv.t_draft, H, D, 2, 2)
+    value = world * T / (pre_ms * 1e-3)
+    dec_value = world * wd.batch / (dec_ms * 1e-3)
+    ver_value = world * wv.batch * wv.t_draft / (ver_ms * 1e-3)
+
+    def roof(bytes_, ms):
+        ach = bytes_ / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": round(ach, 1), "peak": bw_peak, "unit": "GB/s",
+                "frac": round(ach / bw_peak, 4), "peak_source": f"hbm_gbs ({peak_src})"}
+
+    kernels = [{"name": n, "ms": round(m, 5)} for n, m in
+               zip(("kda_chunk_table", "kda_chunk_intra", "kda_chunk_state"), phase_ms)]
+    kernels += [{"name": "kda_recurrent_decode", "ms": round(dec_ms, 5)},
+                {"name": "kda_recurrent_verify", "ms": round(ver_ms, 5)}]
+    tot = sum(k["ms"] for k in kernels)
+    for k in kernels:
+        k["share"] = round(k["ms"] / tot, 4)
+    dominant = max(kernels, key=lambda k: k["ms"])
+
+    roofline = roof(pre_B, pre_ms)
+    roofline.update({"scope": "prefill call (chunk_table + chunk_intra + chunk_state), varlen workload",
+                     "algorithmic_bytes": pre_B, "ms": round(pre_ms, 5), "traffic": None,
+                     "dominant_kernel": dominant["name"]})
+
+    # ---- end to end: host buffers, copies inside the timed region -----------------------------
+    e2e = None
+    if not args.no_e2e:
+        host = {k: pre_h[k].pin_memory() for k in ("q", "k", "v", "g_raw", "b_raw", "cu_seqlens", "state_idx")}
+        host_out = torch.empty(T, H, D, dtype=torch.bfloat16).pin_memory()
+        dbuf = {k: torch.empty_like(pre[k]) for k in host}
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = host_out.numel() * host_out.element_size()
+
+        def e2e_step():
+            for k_ in host:
+                dbuf[k_].copy_(host[k_], non_blocking=True)
+            kda.chunk_prefill(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g_raw"], dbuf["b_raw"], pre["A_log"],
+                              pre["dt_bias"], dbuf["cu_seqlens"], pre["pool"], dbuf["state_idx"], out_pre,
+                              params=p_pre, workspace=ws)
+            host_out.copy_(out_pre, non_blocking=True)
+
+        for _ in range(W):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(dist)
+        a, b = ev(), ev()
+        a.record()
+        for _ in range(K):
+            e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max(dist, a.elapsed_time(b) / K, dev)
+        e2e = {"value": world * T / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+               "scope": "kda_chunk_prefill through the C ABI with pinned host inputs/outputs"}
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline()
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "varlen_prefill_bf16: 8 seqs, lengths U[512,4096] (seed 1001), "
+                               f"T={T}, H=32, d=128, chunk 64",
+                   "io_dtype": "bf16", "out_dtype": "bf16", "state_dtype": "f32", "tokens_per_step": T,
+                   "l2": "no flush: every working set > 129 MB L2", "parallelism": f"replicas x{world}"},
+        "roofline": roofline,
+        "decode": {"value": round(dec_value, 1), "unit": UNIT, "ms": round(dec_ms, 5),
+                   "state_gbs": round(wd.batch * H * 2 * D * D * 4 / (dec_ms * 1e-3) / 1e9, 1),
+                   "roofline": roof(dec_B, dec_ms),
+                   "workload": "decode_bf16: 256 requests x 1 token, H=32, d=128, 512-slot fp32 pool"},
+        "verify": {"value": round(ver_value, 1), "unit": UNIT, "ms": round(ver_ms, 5),
+                   "roofline": roof(ver_B, ver_ms),
+                   "workload": "gdn_verify_bf16: 64 requests x 4 drafts, per-head gate, inter states"},
+        "kernels": kernels,
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,185 @@
+/*
+ * kda.h -- C ABI of libkda: the KDA (Kimi Delta Attention) gated delta-rule recurrence on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The recurrence ("linear_attention", zdszero.github.io, section "KDA：逐通道的遗忘门"), per
+ * head, with row vectors q_t, k_t in R^{1 x d_k}, v_t in R^{1 x d_v} and state S in R^{d_k x d_v}:
+ *
+ *     g_t     = -exp(A_log[h]) * softplus(g_raw_t + dt_bias[h])      (one value per key channel)
+ *     alpha_t = exp(g_t),  beta_t = sigmoid(b_raw_t)
+ *     k_t <- k_t / sqrt(|k_t|^2 + eps),   q_t <- q_t / sqrt(|q_t|^2 + eps) * scale
+ *     S_t     = (I - beta_t k_t^T k_t) Diag(alpha_t) S_{t-1} + beta_t k_t^T v_t
+ *     o_t     = q_t S_t
+ *
+ * Conventions shared by every entry point:
+ *   - Every tensor pointer is caller-owned DEVICE memory (except `p`, a host struct).  The
+ *     library never allocates, frees or keeps a pointer after a call returns.
+ *   - Layouts are row-major with no padding:
+ *       q, k      [T][H][D]    (io_dtype)        v    [T][H][D]  (io_dtype)
+ *       out       [T][H][D]    (out_dtype)
+ *       g_raw     [T][H][D] fp32 for the per-channel (KDA) gate, [T][H] fp32 for the per-head
+ *                 (GDN) gate;  b_raw [T][H] fp32;  A_log [H] fp32;
+ *       dt_bias   [H][D] fp32 (per-channel) or [H] fp32 (per-head); NULL means zero.
+ *       state_pool[num_slots][H][D][D] fp32.  Element [s][h][j][c] holds S[c][j] of slot s: the
+ *                 state is stored transposed (value row j, key channel c contiguous), as in the
+ *                 SGLang pool the pages describe ("linear_attention", section "状态存在哪里").
+ *       state_idx [num_seqs] int32: the slot of each sequence/request.  A negative entry marks a
+ *                 padding row: its outputs are written as zeros and no state is read or written
+ *                 ("ReplaySSM -- buffered output-only decode", yuyanqi.com, section 3.6).  The
+ *                 non-negative entries must be distinct.  An entry >= num_slots is treated as
+ *                 padding and recorded as a device error (kda_check_device_errors).
+ *   - D = d_k = d_v = head_dim.
+ *   - All host-side checks (NULL pointers, sizes, alignment, supported shapes) run before any
+ *     work is enqueued and return a status without touching memory.  Work is then enqueued on
+ *     `stream` and the call returns without synchronising; a launch failure is reported as
+ *     KDA_ERR_CUDA.  No call aborts, throws or prints.
+ *   - The entry points keep no host state between calls and may be called from several host
+ *     threads on different streams.  Calls on the same state slots must be ordered by the caller.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Identical to cudaStream_t; NULL selects the legacy default stream. */
+typedef struct CUstream_st* kda_stream_t;
+/* Identical to cudaEvent_t. */
+typedef struct CUevent_st* kda_event_t;
+
+typedef enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = -1,  /* NULL pointer, negative size, inconsistent sizes */
+    KDA_ERR_UNSUPPORTED = -2,  /* head_dim, chunk_size, dtype or gate combination not built */
+    KDA_ERR_MISALIGNED = -3,   /* a tensor pointer is not 16-byte aligned */
+    KDA_ERR_WORKSPACE = -4,    /* workspace NULL, too small or not 256-byte aligned */
+    KDA_ERR_CUDA = -5,         /* a CUDA runtime call or kernel launch failed */
+    KDA_ERR_DEVICE_CHECK = -6  /* kda_check_device_errors found a recorded argument error */
+} kda_status;
+
+typedef enum kda_dtype { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+typedef enum kda_gate_kind {
+    KDA_GATE_PER_CHANNEL = 0,  /* KDA: one decay per key channel */
+    KDA_GATE_PER_HEAD = 1      /* GDN: one scalar decay per head ("linear_attention", "Gated DeltaNet") */
+} kda_gate_kind;
+
+typedef struct kda_params {
+    int32_t num_heads;          /* H >= 1 */
+    int32_t head_dim;           /* D = d_k = d_v: 16, 32, 64 or 128 */
+    int32_t io_dtype;           /* kda_dtype of q, k, v */
+    int32_t out_dtype;          /* kda_dtype of out */
+    int32_t gate_kind;          /* kda_gate_kind */
+    int32_t chunk_size;         /* prefill chunk length: 16, 32 or 64 (<= 64, multiple of 16) */
+    int32_t use_lower_bound;    /* 0: g = -exp(A_log) * softplus(x)
+                                   1: safe gate g = lower_bound * sigmoid(exp(A_log) * x)
+                                   ("linear_attention", section "实例：Kimi K3") */
+    float lower_bound;          /* e.g. -5; used when use_lower_bound = 1 */
+    float scale;                /* q scale after normalisation; <= 0 selects head_dim^{-1/2} */
+    float l2_eps;               /* 1e-6 ("ReplaySSM", section 3.10) */
+    float softplus_threshold;   /* 20: softplus(x) = x above it ("PR #26888 report") */
+} kda_params;
+
+/* Fill `p` with the pages' defaults: bf16 inputs and output, per-channel gate, chunk 64,
+ * no lower bound, scale = head_dim^{-1/2}, eps = 1e-6, softplus threshold 20. */
+void kda_params_init(kda_params* p, int32_t num_heads, int32_t head_dim);
+
+/* Static description of a status code (never NULL). */
+const char* kda_status_string(int32_t status);
+
+/*
+ * Chunkwise-parallel prefill over packed varlen sequences ("linear_attention", sections
+ * "矩阵（并行）形式" and "两种计算形态"; the interface mirrors chunk_kda of "KDA inference
+ * components", section 4.1, with the gate activation and the q/k L2 norm always fused).
+ *
+ * Sequence i holds tokens cu_seqlens[i] .. cu_seqlens[i+1]-1 of the packed [T][H][..] inputs
+ * and starts from state_pool[state_idx[i]]; the final state is written back to the same slot.
+ * Each sequence is cut into chunks of p->chunk_size tokens starting at its first token.
+ *   cu_seqlens    device int32 [num_seqs + 1], non-decreasing, cu_seqlens[0] = 0,
+ *                 cu_seqlens[num_seqs] = total_tokens.  Never read back to the host; a malformed
+ *                 table is clamped and recorded as a device error.
+ *   total_tokens  T >= 0 (the number of rows of q, k, v, g_raw, b_raw, out).
+ *   workspace     device scratch of at least kda_chunk_prefill_workspace_size(...) bytes,
+ *                 256-byte aligned, owned by the caller; its contents need not be initialised
+ *                 and are garbage afterwards.  It must not be shared with a call that overlaps
+ *                 in time.
+ * T = 0 or num_seqs = 0 is a no-op.
+ */
+size_t kda_chunk_prefill_workspace_size(const kda_params* p, int32_t num_seqs, int64_t total_tokens);
+
+int32_t kda_chunk_prefill(const kda_params* p,
+                          const void* q, const void* k, const void* v,
+                          const float* g_raw, const float* b_raw,
+                          const float* A_log, const float* dt_bias,
+                          const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                          float* state_pool, int64_t num_slots, const int32_t* state_idx,
+                          void* out,
+                          void* workspace, size_t workspace_bytes,
+                          kda_stream_t stream);
+
+/*
+ * kda_chunk_prefill with per-phase timing: the same work, plus caller-created CUDA events
+ * recorded on `stream` around its kernels: events[0] before the chunk-table kernel, events[1]
+ * after it, events[2] after the intra-chunk kernel, events[3] after the inter-chunk state pass.
+ * `events` must hold KDA_PREFILL_PHASE_EVENTS valid event handles (owned by the caller).
+ */
+#define KDA_PREFILL_PHASE_EVENTS 4
+int32_t kda_chunk_prefill_timed(const kda_params* p,
+                                const void* q, const void* k, const void* v,
+                                const float* g_raw, const float* b_raw,
+                                const float* A_log, const float* dt_bias,
+                                const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                                float* state_pool, int64_t num_slots, const int32_t* state_idx,
+                                void* out,
+                                void* workspace, size_t workspace_bytes,
+                                kda_stream_t stream, kda_event_t const* events);
+
+/*
+ * Single-token recurrent decode against the pooled state, updated in place ("linear_attention",
+ * section "两种计算形态", the fused recurrent kernel; per-token steps of section "Gated DeltaNet":
+ * decay, predict, error, write, read).  Request b is token b of the [batch][H][..] inputs.
+ */
+int32_t kda_recurrent_decode(const kda_params* p,
+                             const void* q, const void* k, const void* v,
+                             const float* g_raw, const float* b_raw,
+                             const float* A_log, const float* dt_bias,
+                             int32_t batch,
+                             float* state_pool, int64_t num_slots, const int32_t* state_idx,
+                             void* out,
+                             kda_stream_t stream);
+
+/*
+ * Multi-token verify ("PR #26888 report": target_verify with disable_state_update and an
+ * intermediate-state buffer; "linear_attention", section "prefix cache 与投机解码").
+ * Request b owns tokens b*t_draft .. b*t_draft + t_draft - 1 of the inputs (request-major).
+ * The pool is only read.  The state after draft token t of request b is written to
+ *   inter_states [batch][t_draft][H][D][D] fp32 (same transposed layout as the pool),
+ * and out is [batch * t_draft][H][D].  Padding rows (state_idx < 0) write zero outputs and
+ * leave their inter_states untouched.  1 <= t_draft <= 16.
+ */
+int32_t kda_recurrent_verify(const kda_params* p,
+                             const void* q, const void* k, const void* v,
+                             const float* g_raw, const float* b_raw,
+                             const float* A_log, const float* dt_bias,
+                             int32_t batch, int32_t t_draft,
+                             const float* state_pool, int64_t num_slots, const int32_t* state_idx,
+                             float* inter_states, void* out,
+                             kda_stream_t stream);
+
+/*
+ * Synchronise `stream`, then read and clear the device error word that the kernels set when
+ * they meet an out-of-range state_idx or a malformed cu_seqlens.  *code receives the first
+ * recorded code (0 when none) for the current device.  Returns KDA_OK when no error was
+ * recorded, KDA_ERR_DEVICE_CHECK when one was, KDA_ERR_CUDA when the synchronisation failed.
+ */
+int32_t kda_check_device_errors(kda_stream_t stream, int32_t* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

@@ -1,0 +1,695 @@
+// kda_prefill.cu -- chunkwise-parallel KDA prefill over packed varlen sequences (fp32 SIMT path).
+//
+// Algorithm ("linear_attention", zdszero.github.io, sections "矩阵（并行）形式" and
+// "两种计算形态"): each sequence is cut into chunks of C tokens.  For a chunk of L tokens with
+// per-channel cumulative log decay G_r = sum_{i<=r} g_i and entry state S0:
+//   A[r][j] = beta_r sum_c k_r[c] k_j[c] e^{G_r[c]-G_j[c]}       (j <  r)
+//   P[r][j] =        sum_c q_r[c] k_j[c] e^{G_r[c]-G_j[c]}       (j <= r)
+//   U = (I + A)^{-1} diag(beta) V,   W = (I + A)^{-1} diag(beta) (K o e^{G})   (forward substitution)
+//   Delta = U - W S0;   O = (Q o e^{G}) S0 + P Delta
+//   S_L   = Diag(e^{G_L}) S0 + (K o e^{G_L - G})^T Delta
+//
+// Three kernels, all on the caller's stream, no host synchronisation:
+//   chunk_table_kernel   builds the chunk list from the device cu_seqlens;
+//   chunk_intra_kernel   one CTA per (chunk, head): everything that does not depend on S0
+//                        (W, U, Q o e^G, K o e^{G_L-G}, P, e^{G_L}) into the workspace;
+//   chunk_state_kernel   one CTA per (sequence, head, value tile): the serial pass over the
+//                        sequence's chunks, keeping its slice of S on chip.
+//
+// Overflow-free decay algebra.  With these gates g reaches tens per token, so e^{-G} overflows
+// fp32 long before a chunk ends.  No decay factor here is ever formed from an exponent > 0:
+//   * alpha = e^{g} <= 1 is computed once per (token, channel);
+//   * every decay e^{G_r - G_j} (r >= j) is a product of alphas, split at 16-row sub-block
+//     boundaries: r in block I, j in block J < I  ->  Rin_I(r) * M_IJ * Rout_J(j), with
+//     Rin the in-block prefix product up to r, Rout the in-block suffix product after j and
+//     M_IJ the product of the whole blocks strictly between them; inside a diagonal block the
+//     running product is accumulated token by token.
+// Products of factors in (0, 1] cannot overflow and lose at most one rounding per factor, so the
+// fp32 path keeps the 1e-5 relative accuracy the fp32 configuration needs.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+__device__ int32_t g_prefill_error = 0;
+__device__ __forceinline__ void record_error(int32_t code) { atomicCAS(&g_prefill_error, 0, code); }
+
+constexpr int kSub = 16;  // sub-block length of the decay split
+
+// ---- workspace layout ----------------------------------------------------------------------
+// [chunk table: 3 * max_chunks + (N + 1) int32, padded to 256 B]
+// [per (chunk, head): W C*D | Qbar C*D | Ktil C*D | U C*D | P C*C | gL D  floats, padded to 64]
+struct WsLayout {
+    int64_t max_chunks;
+    size_t table_bytes;
+    size_t per_chunk_head;  // floats
+    size_t total_bytes;
+};
+
+__host__ __device__ inline size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
+
+WsLayout ws_layout(int C, int D, int H, int32_t N, int64_t T)
+{
+    WsLayout w;
+    w.max_chunks = (T + C - 1) / C + N;
+    w.table_bytes = round_up(sizeof(int32_t) * (size_t)(3 * w.max_chunks + N + 1), 256);
+    w.per_chunk_head = round_up((size_t)4 * C * D + (size_t)C * C + D, 64);
+    w.total_bytes = w.table_bytes + sizeof(float) * w.per_chunk_head * (size_t)w.max_chunks * H;
+    return w;
+}
+
+// ---- chunk table -----------------------------------------------------------------------------
+// One CTA of 1024 threads.  chunk i of the packed batch covers tokens
+// chunk_start[i] .. chunk_start[i] + chunk_len[i] - 1 of sequence chunk_seq[i]; the chunks of
+// sequence s are seq_off[s] .. seq_off[s+1]-1 and seq_off[N] is the number of chunks.
+__global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* __restrict__ cu, int32_t N, int64_t T,
+                                                           int C, int64_t max_chunks,
+                                                           int32_t* chunk_seq, int32_t* chunk_start,
+                                                           int32_t* chunk_len, int32_t* seq_off)
+{
+    __shared__ int32_t s_warp[32];
+    __shared__ int32_t s_base;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) s_base = 0;
+    __syncthreads();
+    for (int32_t base = 0; base < N; base += blockDim.x) {
+        const int32_t i = base + tid;
+        int64_t s0 = 0, s1 = 0;
+        int32_t n = 0;
+        if (i < N) {
+            s0 = cu[i];
+            s1 = cu[i + 1];
+            const bool bad = s0 < 0 || s1 < s0 || s1 > T || (i == 0 && s0 != 0) || (i == N - 1 && s1 != T);
+            if (bad) {
+                record_error(kDevErrSeqlens);
+                s0 = s0 < 0 ? 0 : (s0 > T ? T : s0);
+                s1 = s1 < s0 ? s0 : (s1 > T ? T : s1);
+            }
+            n = (int32_t)((s1 - s0 + C - 1) / C);
+        }
+        // inclusive scan of n over the CTA
+        int32_t x = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        if (lane == 31) s_warp[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int32_t w = lane < (int)(blockDim.x >> 5) ? s_warp[lane] : 0;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int32_t y = __shfl_up_sync(0xffffffffu, w, off);
+                if (lane >= off) w += y;
+            }
+            s_warp[lane] = w;
+        }
+        __syncthreads();
+        const int32_t incl = x + (warp > 0 ? s_warp[warp - 1] : 0);
+        const int32_t off0 = s_base + incl - n;
+        if (i < N) {
+            seq_off[i] = off0;
+            for (int32_t m = 0; m < n; ++m) {
+                const int64_t c = (int64_t)off0 + m;
+                if (c >= max_chunks) {
+                    record_error(kDevErrSeqlens);
+                    break;
+                }
+                const int64_t st = s0 + (int64_t)m * C;
+                chunk_seq[c] = i;
+                chunk_start[c] = (int32_t)st;
+                chunk_len[c] = (int32_t)((s1 - st) < C ? (s1 - st) : C);
+            }
+        }
+        __syncthreads();
+        if (tid == blockDim.x - 1) s_base = off0 + n;
+        __syncthreads();
+    }
+    if (tid == 0) seq_off[N] = s_base;
+}
+
+// ---- intra-chunk kernel ----------------------------------------------------------------------
+struct IntraArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g_raw;
+    const float* b_raw;
+    const float* A_log;
+    const float* dt_bias;
+    const int32_t* chunk_seq;
+    const int32_t* chunk_start;
+    const int32_t* chunk_len;
+    const int32_t* seq_off;   // seq_off[N] = number of chunks
+    const int32_t* state_idx;
+    int64_t num_slots;
+    int64_t max_chunks;
+    int32_t N;
+    int H;
+    GateParams gp;
+    float* ws;                // per-(chunk, head) records
+    size_t ws_stride;         // floats per record
+};
+
+template <int C, int D>
+struct IntraShape {
+    static constexpr int THREADS = (2 * D > C ? 2 * D : C) < 64 ? 64 : (2 * D > C ? 2 * D : C);
+    static constexpr int NB = C / kSub;           // sub-blocks per chunk
+    static constexpr int NCG = THREADS / C;        // column groups per row j (diagonal blocks)
+    static constexpr int CPT = D / NCG;            // columns per thread (diagonal blocks)
+    static constexpr int PADC = C + 1;
+    static_assert(C % kSub == 0, "chunk must be a multiple of 16");
+    static_assert(NCG >= 1 && D % (4 * NCG) == 0, "column split");
+    static_assert(THREADS >= 2 * D && THREADS >= C, "threads");
+    // shared memory (floats)
+    static constexpr size_t OFF_AL = 0;                       // alpha [C][D]
+    static constexpr size_t OFF_K = OFF_AL + (size_t)C * D;   // k_hat -> k o Rin  [C][D]
+    static constexpr size_t OFF_Q = OFF_K + (size_t)C * D;    // q_hat -> q o Rin  [C][D]
+    static constexpr size_t OFF_KOT = OFF_Q + (size_t)C * D;  // (k o Rout)^T [D][C+1]
+    static constexpr size_t OFF_A = OFF_KOT + (size_t)D * PADC;
+    static constexpr size_t OFF_P = OFF_A + (size_t)C * PADC;
+    static constexpr size_t OFF_BP = OFF_P + (size_t)C * PADC;  // block products [NB][D]
+    static constexpr size_t OFF_BETA = OFF_BP + (size_t)NB * D;
+    static constexpr size_t OFF_RED = OFF_BETA + C;            // row norms [2][C]
+    static constexpr size_t FLOATS = OFF_RED + 2 * C;
+    static constexpr size_t BYTES = FLOATS * sizeof(float);
+};
+
+template <int C, int D, typename TIn>
+__global__ void __launch_bounds__(IntraShape<C, D>::THREADS, 1) chunk_intra_kernel(const IntraArgs a)
+{
+    using Sh = IntraShape<C, D>;
+    constexpr int THREADS = Sh::THREADS, NB = Sh::NB, NCG = Sh::NCG, CPT = Sh::CPT, PADC = Sh::PADC;
+    extern __shared__ float4 smem4[];
+    float* sm = reinterpret_cast<float*>(smem4);
+    float* s_al = sm + Sh::OFF_AL;
+    float* s_k = sm + Sh::OFF_K;
+    float* s_q = sm + Sh::OFF_Q;
+    float* s_koT = sm + Sh::OFF_KOT;
+    float* s_A = sm + Sh::OFF_A;
+    float* s_P = sm + Sh::OFF_P;
+    float* s_bp = sm + Sh::OFF_BP;
+    float* s_beta = sm + Sh::OFF_BETA;
+    float* s_rn = sm + Sh::OFF_RED;
+
+    const int64_t ch = blockIdx.x;
+    const int h = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int64_t nch = a.seq_off[a.N];
+    if (nch > a.max_chunks) nch = a.max_chunks;
+    if (ch >= nch) return;
+    const int32_t seq = a.chunk_seq[ch];
+    const int64_t slot = a.state_idx[seq];
+    if (slot < 0 || slot >= a.num_slots) return;  // padding row: the state pass writes zeros
+    const int64_t t0 = a.chunk_start[ch];
+    const int L = a.chunk_len[ch];
+    const int H = a.H;
+    const TIn* qp = reinterpret_cast<const TIn*>(a.q);
+    const TIn* kp = reinterpret_cast<const TIn*>(a.k);
+    const TIn* vp = reinterpret_cast<const TIn*>(a.v);
+    const float rate = expf(a.A_log[h]);
+
+    // 1. load k, q, alpha = e^{g}; rows past the chunk end are k = q = 0, alpha = 1, beta = 0
+    for (int e = tid; e < C * D; e += THREADS) {
+        const int r = e / D, c = e % D;
+        float kv = 0.f, qv = 0.f, al = 1.f;
+        if (r < L) {
+            const size_t idx = ((size_t)(t0 + r) * H + h) * D + c;
+            kv = to_f32(kp[idx]);
+            qv = to_f32(qp[idx]);
+            const float x = a.g_raw[idx] + (a.dt_bias ? a.dt_bias[(size_t)h * D + c] : 0.f);
+            al = expf(gate_log_decay(x, rate, a.gp));
+        }
+        s_k[e] = kv;
+        s_q[e] = qv;
+        s_al[e] = al;
+    }
+    for (int r = tid; r < C; r += THREADS)
+        s_beta[r] = r < L ? sigmoid_f32(a.b_raw[(size_t)(t0 + r) * H + h]) : 0.f;
+    __syncthreads();
+
+    // 2. L2-normalise the rows of k and q (one warp per row)
+    for (int r = warp; r < C; r += THREADS / 32) {
+        float kk = 0.f, qq = 0.f;
+        for (int c = lane; c < D; c += 32) {
+            kk += s_k[r * D + c] * s_k[r * D + c];
+            qq += s_q[r * D + c] * s_q[r * D + c];
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            kk += __shfl_xor_sync(0xffffffffu, kk, off);
+            qq += __shfl_xor_sync(0xffffffffu, qq, off);
+        }
+        if (lane == 0) {
+            s_rn[r] = 1.0f / sqrtf(kk + a.gp.l2_eps);
+            s_rn[C + r] = a.gp.scale / sqrtf(qq + a.gp.l2_eps);
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < C * D; e += THREADS) {
+        const int r = e / D;
+        s_k[e] *= s_rn[r];
+        s_q[e] *= s_rn[C + r];
+    }
+    for (int e = tid; e < C * PADC; e += THREADS) {
+        s_A[e] = 0.f;
+        s_P[e] = 0.f;
+    }
+    __syncthreads();
+
+    // 3. diagonal sub-blocks: running product of alphas, one (row j, column group) per thread
+    {
+        const int j = tid / NCG;       // 0 .. C-1
+        const int cg = tid % NCG;
+        const int blk0 = (j / kSub) * kSub;
+        float kd[CPT];
+#pragma unroll
+        for (int m = 0; m < CPT / 4; ++m) {
+            const float4 v4 = *reinterpret_cast<const float4*>(&s_k[j * D + 4 * cg + 4 * NCG * m]);
+            kd[4 * m + 0] = v4.x; kd[4 * m + 1] = v4.y; kd[4 * m + 2] = v4.z; kd[4 * m + 3] = v4.w;
+        }
+#pragma unroll 1
+        for (int rr = 0; rr < kSub; ++rr) {
+            const int r = blk0 + rr;
+            const bool act = r >= j;
+            float pa = 0.f, pp = 0.f;
+#pragma unroll
+            for (int m = 0; m < CPT / 4; ++m) {
+                const int c = 4 * cg + 4 * NCG * m;
+                const float4 al4 = *reinterpret_cast<const float4*>(&s_al[r * D + c]);
+                const float4 k4 = *reinterpret_cast<const float4*>(&s_k[r * D + c]);
+                const float4 q4 = *reinterpret_cast<const float4*>(&s_q[r * D + c]);
+                if (r > j) {
+                    kd[4 * m + 0] *= al4.x; kd[4 * m + 1] *= al4.y;
+                    kd[4 * m + 2] *= al4.z; kd[4 * m + 3] *= al4.w;
+                }
+                pa = fmaf(k4.x, kd[4 * m + 0], pa); pa = fmaf(k4.y, kd[4 * m + 1], pa);
+                pa = fmaf(k4.z, kd[4 * m + 2], pa); pa = fmaf(k4.w, kd[4 * m + 3], pa);
+                pp = fmaf(q4.x, kd[4 * m + 0], pp); pp = fmaf(q4.y, kd[4 * m + 1], pp);
+                pp = fmaf(q4.z, kd[4 * m + 2], pp); pp = fmaf(q4.w, kd[4 * m + 3], pp);
+            }
+#pragma unroll
+            for (int off = NCG / 2; off > 0; off >>= 1) {
+                pa += __shfl_xor_sync(0xffffffffu, pa, off);
+                pp += __shfl_xor_sync(0xffffffffu, pp, off);
+            }
+            if (act && cg == 0) {
+                if (r > j) s_A[r * PADC + j] = s_beta[r] * pa;
+                s_P[r * PADC + j] = pp;
+            }
+        }
+    }
+    __syncthreads();
+
+    // 4. per-column sub-block products: k o Rin -> s_k, q o Rin -> s_q, (k o Rout)^T -> s_koT
+    for (int c = tid; c < D; c += THREADS) {
+        for (int blk = 0; blk < NB; ++blk) {
+            float rout = 1.f;
+            for (int rr = kSub - 1; rr >= 0; --rr) {
+                const int r = blk * kSub + rr;
+                s_koT[c * PADC + r] = s_k[r * D + c] * rout;
+                rout *= s_al[r * D + c];
+            }
+            s_bp[blk * D + c] = rout;
+            float rin = 1.f;
+            for (int rr = 0; rr < kSub; ++rr) {
+                const int r = blk * kSub + rr;
+                rin *= s_al[r * D + c];
+                s_k[r * D + c] *= rin;
+                s_q[r * D + c] *= rin;
+            }
+        }
+    }
+    __syncthreads();
+
+    // 5. off-diagonal sub-blocks: A[r][j] = beta_r sum_c kin[r][c] M_IJ[c] kout[j][c], same for P
+    for (int e = tid; e < NB * (NB - 1) / 2 * kSub * kSub; e += THREADS) {
+        int pair = e / (kSub * kSub);
+        const int within = e % (kSub * kSub);
+        int I = 1, J = 0;
+        {   // enumerate (I, J) with J < I
+            int cnt = pair;
+            for (I = 1; I < NB; ++I) {
+                if (cnt < I) { J = cnt; break; }
+                cnt -= I;
+            }
+        }
+        const int r = I * kSub + within / kSub;
+        const int j = J * kSub + within % kSub;
+        float pa = 0.f, pp = 0.f;
+        for (int c = 0; c < D; ++c) {
+            float m = 1.f;
+            for (int bb = J + 1; bb < I; ++bb) m *= s_bp[bb * D + c];
+            const float ko = s_koT[c * PADC + j] * m;
+            pa = fmaf(s_k[r * D + c], ko, pa);
+            pp = fmaf(s_q[r * D + c], ko, pp);
+        }
+        s_A[r * PADC + j] = s_beta[r] * pa;
+        s_P[r * PADC + j] = pp;
+    }
+    __syncthreads();
+
+    float* rec = a.ws + ((size_t)ch * H + h) * a.ws_stride;
+    float* wW = rec;
+    float* wQ = rec + (size_t)C * D;
+    float* wK = rec + (size_t)2 * C * D;
+    float* wU = rec + (size_t)3 * C * D;
+    float* wP = rec + (size_t)4 * C * D;
+    float* wG = wP + (size_t)C * C;
+
+    // 6. forward substitution, one column of [U | W] per thread: x_r = rhs_r - sum_{j<r} A[r][j] x_j
+    if (tid < 2 * D) {
+        const bool isU = tid < D;
+        const int c = isU ? tid : tid - D;
+        float x[C];
+#pragma unroll
+        for (int r = 0; r < C; ++r) {
+            float rhs;
+            if (isU) {
+                rhs = r < L ? s_beta[r] * to_f32(vp[((size_t)(t0 + r) * H + h) * D + c]) : 0.f;
+            } else {
+                float eb = 1.f;  // e^{G} up to the start of r's sub-block
+                for (int bb = 0; bb < r / kSub; ++bb) eb *= s_bp[bb * D + c];
+                rhs = s_beta[r] * s_k[r * D + c] * eb;
+            }
+#pragma unroll
+            for (int jj = 0; jj < r; ++jj) rhs = fmaf(-s_A[r * PADC + jj], x[jj], rhs);
+            x[r] = rhs;
+            (isU ? wU : wW)[(size_t)r * D + c] = rhs;
+        }
+    }
+    // 7. Qbar = q o e^{G}, Ktil = k o e^{G_L - G}, P, e^{G_L}
+    for (int e = tid; e < C * D; e += THREADS) {
+        const int r = e / D, c = e % D;
+        const int blk = r / kSub;
+        float eb = 1.f, ea = 1.f;
+        for (int bb = 0; bb < blk; ++bb) eb *= s_bp[bb * D + c];
+        for (int bb = blk + 1; bb < NB; ++bb) ea *= s_bp[bb * D + c];
+        wQ[e] = s_q[e] * eb;
+        wK[e] = s_koT[c * PADC + r] * ea;
+    }
+    for (int e = tid; e < C * C; e += THREADS) wP[e] = s_P[(e / C) * PADC + (e % C)];
+    for (int c = tid; c < D; c += THREADS) {
+        float g = 1.f;
+        for (int bb = 0; bb < NB; ++bb) g *= s_bp[bb * D + c];
+        wG[c] = g;
+    }
+}
+
+// ---- inter-chunk state pass ----------------------------------------------------------------------
+struct StateArgs {
+    const int32_t* chunk_start;
+    const int32_t* chunk_len;
+    const int32_t* seq_off;
+    const int32_t* cu;
+    const int32_t* state_idx;
+    float* pool;
+    int64_t num_slots;
+    int64_t max_chunks;
+    int64_t T;
+    int32_t N;
+    int H;
+    const float* ws;
+    size_t ws_stride;
+    void* out;
+};
+
+template <int C, int D, int NV>
+struct StateShape {
+    static constexpr int THREADS = 256;
+    static constexpr int TV = NV;              // threads along v
+    static constexpr int TR = THREADS / NV;    // threads along r (or c)
+    static constexpr int RPT = C / TR;         // rows per thread (Delta, O)
+    static constexpr int CPT = D / TR;         // key channels per thread (S update)
+    static_assert(THREADS % NV == 0 && C % TR == 0 && D % TR == 0, "tiling");
+    static constexpr size_t OFF_S = 0;                          // S [D][NV]
+    static constexpr size_t OFF_W = OFF_S + (size_t)D * NV;     // W [C][D]
+    static constexpr size_t OFF_Q = OFF_W + (size_t)C * D;      // Qbar [C][D]
+    static constexpr size_t OFF_K = OFF_Q + (size_t)C * D;      // Ktil [C][D]
+    static constexpr size_t OFF_P = OFF_K + (size_t)C * D;      // P [C][C]
+    static constexpr size_t OFF_U = OFF_P + (size_t)C * C;      // U -> Delta [C][NV]
+    static constexpr size_t OFF_G = OFF_U + (size_t)C * NV;     // e^{G_L} [D]
+    static constexpr size_t FLOATS = OFF_G + D;
+    static constexpr size_t BYTES = FLOATS * sizeof(float);
+};
+
+template <int C, int D, int NV, typename TOut>
+__global__ void __launch_bounds__(256, 1) chunk_state_kernel(const StateArgs a)
+{
+    using Sh = StateShape<C, D, NV>;
+    constexpr int THREADS = Sh::THREADS, TR = Sh::TR, RPT = Sh::RPT, CPT = Sh::CPT;
+    extern __shared__ float4 smem4[];
+    float* sm = reinterpret_cast<float*>(smem4);
+    float* s_S = sm + Sh::OFF_S;
+    float* s_W = sm + Sh::OFF_W;
+    float* s_Q = sm + Sh::OFF_Q;
+    float* s_K = sm + Sh::OFF_K;
+    float* s_P = sm + Sh::OFF_P;
+    float* s_U = sm + Sh::OFF_U;
+    float* s_G = sm + Sh::OFF_G;
+
+    const int seq = blockIdx.x;
+    const int h = blockIdx.y;
+    const int v0 = blockIdx.z * NV;
+    const int tid = threadIdx.x;
+    const int tv = tid % NV, tr = tid / NV;
+    const int H = a.H;
+    TOut* out = reinterpret_cast<TOut*>(a.out);
+
+    int64_t slot = a.state_idx[seq];
+    if (slot >= a.num_slots) {
+        if (tid == 0 && blockIdx.y == 0 && blockIdx.z == 0) record_error(kDevErrStateIndex);
+        slot = -1;
+    }
+    int64_t c_begin = a.seq_off[seq], c_end = a.seq_off[seq + 1];
+    if (c_end > a.max_chunks) c_end = a.max_chunks;
+    if (slot < 0) {  // padding row: zero outputs over the sequence's tokens
+        int64_t s0 = a.cu[seq], s1 = a.cu[seq + 1];
+        s0 = s0 < 0 ? 0 : (s0 > a.T ? a.T : s0);
+        s1 = s1 < s0 ? s0 : (s1 > a.T ? a.T : s1);
+        for (int64_t e = tid; e < (s1 - s0) * NV; e += THREADS) {
+            const int64_t t = s0 + e / NV;
+            out[((size_t)t * H + h) * D + v0 + e % NV] = from_f32<TOut>(0.f);
+        }
+        return;
+    }
+    float* Sg = a.pool + ((size_t)slot * H + h) * (size_t)D * D;
+    for (int e = tid; e < D * NV; e += THREADS) {   // S[c][v] = pool[v0 + v][c]
+        const int v = e / D, c = e % D;
+        s_S[c * NV + v] = Sg[(size_t)(v0 + v) * D + c];
+    }
+
+    for (int64_t ch = c_begin; ch < c_end; ++ch) {
+        const float* rec = a.ws + ((size_t)ch * H + h) * a.ws_stride;
+        const int64_t t0 = a.chunk_start[ch];
+        const int L = a.chunk_len[ch];
+        __syncthreads();  // previous chunk done with the staging buffers
+        {
+            const float4* src = reinterpret_cast<const float4*>(rec);
+            float4* dW = reinterpret_cast<float4*>(s_W);
+            for (int e = tid; e < 3 * C * D / 4; e += THREADS) dW[e] = src[e];  // W, Qbar, Ktil contiguous
+            const float4* srcP = reinterpret_cast<const float4*>(rec + (size_t)4 * C * D);
+            float4* dP = reinterpret_cast<float4*>(s_P);
+            for (int e = tid; e < C * C / 4; e += THREADS) dP[e] = srcP[e];
+            for (int e = tid; e < C * NV; e += THREADS) {
+                const int r = e / NV, v = e % NV;
+                s_U[e] = rec[(size_t)3 * C * D + (size_t)r * D + v0 + v];
+            }
+            for (int e = tid; e < D; e += THREADS) s_G[e] = rec[(size_t)4 * C * D + (size_t)C * C + e];
+        }
+        __syncthreads();
+        // Delta = U - W S
+        {
+            float acc[RPT];
+#pragma unroll
+            for (int i = 0; i < RPT; ++i) acc[i] = s_U[(tr + TR * i) * NV + tv];
+            for (int c = 0; c < D; c += 4) {
+                const float s0 = s_S[(c + 0) * NV + tv], s1 = s_S[(c + 1) * NV + tv];
+                const float s2 = s_S[(c + 2) * NV + tv], s3 = s_S[(c + 3) * NV + tv];
+#pragma unroll
+                for (int i = 0; i < RPT; ++i) {
+                    const float4 w = *reinterpret_cast<const float4*>(&s_W[(tr + TR * i) * D + c]);
+                    acc[i] = fmaf(-w.x, s0, acc[i]); acc[i] = fmaf(-w.y, s1, acc[i]);
+                    acc[i] = fmaf(-w.z, s2, acc[i]); acc[i] = fmaf(-w.w, s3, acc[i]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < RPT; ++i) s_U[(tr + TR * i) * NV + tv] = acc[i];
+        }
+        __syncthreads();
+        // O = Qbar S + P Delta (rows past the chunk end are not stored)
+        {
+            float acc[RPT];
+#pragma unroll
+            for (int i = 0; i < RPT; ++i) acc[i] = 0.f;
+            for (int c = 0; c < D; c += 4) {
+                const float s0 = s_S[(c + 0) * NV + tv], s1 = s_S[(c + 1) * NV + tv];
+                const float s2 = s_S[(c + 2) * NV + tv], s3 = s_S[(c + 3) * NV + tv];
+#pragma unroll
+                for (int i = 0; i < RPT; ++i) {
+                    const float4 qv = *reinterpret_cast<const float4*>(&s_Q[(tr + TR * i) * D + c]);
+                    acc[i] = fmaf(qv.x, s0, acc[i]); acc[i] = fmaf(qv.y, s1, acc[i]);
+                    acc[i] = fmaf(qv.z, s2, acc[i]); acc[i] = fmaf(qv.w, s3, acc[i]);
+                }
+            }
+            for (int j = 0; j < C; ++j) {
+                const float dj = s_U[j * NV + tv];
+#pragma unroll
+                for (int i = 0; i < RPT; ++i) {
+                    const int r = tr + TR * i;
+                    if (j <= r) acc[i] = fmaf(s_P[r * C + j], dj, acc[i]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < RPT; ++i) {
+                const int r = tr + TR * i;
+                if (r < L) out[((size_t)(t0 + r) * H + h) * D + v0 + tv] = from_f32<TOut>(acc[i]);
+            }
+        }
+        // S <- Diag(e^{G_L}) S + Ktil^T Delta
+        {
+            float acc[CPT];
+#pragma unroll
+            for (int i = 0; i < CPT; ++i) {
+                const int c = tr + TR * i;
+                acc[i] = s_G[c] * s_S[c * NV + tv];
+            }
+            for (int r = 0; r < C; ++r) {
+                const float dr = s_U[r * NV + tv];
+#pragma unroll
+                for (int i = 0; i < CPT; ++i) acc[i] = fmaf(s_K[r * D + tr + TR * i], dr, acc[i]);
+            }
+            __syncthreads();  // every thread has finished reading the old S
+#pragma unroll
+            for (int i = 0; i < CPT; ++i) s_S[(tr + TR * i) * NV + tv] = acc[i];
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < D * NV; e += THREADS) {
+        const int v = e / D, c = e % D;
+        Sg[(size_t)(v0 + v) * D + c] = s_S[c * NV + v];
+    }
+}
+
+// ---- host-side dispatch --------------------------------------------------------------------------
+template <int C, int D, typename TIn, typename TOut>
+cudaError_t run_prefill(const kda_params& p, const GateParams& gp, const void* q, const void* k,
+                        const void* v, const float* g_raw, const float* b_raw, const float* A_log,
+                        const float* dt_bias, const int32_t* cu, int32_t N, int64_t T, float* pool,
+                        int64_t num_slots, const int32_t* state_idx, void* out, void* workspace,
+                        cudaStream_t stream, const cudaEvent_t* ev)
+{
+    const int H = p.num_heads;
+    const WsLayout w = ws_layout(C, D, H, N, T);
+    int32_t* tab = reinterpret_cast<int32_t*>(workspace);
+    int32_t* chunk_seq = tab;
+    int32_t* chunk_start = tab + w.max_chunks;
+    int32_t* chunk_len = tab + 2 * w.max_chunks;
+    int32_t* seq_off = tab + 3 * w.max_chunks;
+    float* ws = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + w.table_bytes);
+
+    cudaError_t e;
+    if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
+    chunk_table_kernel<<<1, 1024, 0, stream>>>(cu, N, T, C, w.max_chunks, chunk_seq, chunk_start, chunk_len, seq_off);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return e;
+
+    IntraArgs ia;
+    ia.q = q; ia.k = k; ia.v = v; ia.g_raw = g_raw; ia.b_raw = b_raw; ia.A_log = A_log; ia.dt_bias = dt_bias;
+    ia.chunk_seq = chunk_seq; ia.chunk_start = chunk_start; ia.chunk_len = chunk_len; ia.seq_off = seq_off;
+    ia.state_idx = state_idx; ia.num_slots = num_slots; ia.max_chunks = w.max_chunks; ia.N = N; ia.H = H;
+    ia.gp = gp; ia.ws = ws; ia.ws_stride = w.per_chunk_head;
+    using IS = IntraShape<C, D>;
+    auto intra = chunk_intra_kernel<C, D, TIn>;
+    e = cudaFuncSetAttribute(intra, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)IS::BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 gi((unsigned)w.max_chunks, (unsigned)H);
+    intra<<<gi, IS::THREADS, IS::BYTES, stream>>>(ia);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return e;
+
+    constexpr int NV = D < 32 ? D : 32;
+    StateArgs sa;
+    sa.chunk_start = chunk_start; sa.chunk_len = chunk_len; sa.seq_off = seq_off; sa.cu = cu;
+    sa.state_idx = state_idx; sa.pool = pool; sa.num_slots = num_slots; sa.max_chunks = w.max_chunks;
+    sa.T = T; sa.N = N; sa.H = H; sa.ws = ws; sa.ws_stride = w.per_chunk_head; sa.out = out;
+    using SS = StateShape<C, D, NV>;
+    auto state = chunk_state_kernel<C, D, NV, TOut>;
+    e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SS::BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 gs((unsigned)N, (unsigned)H, (unsigned)(D / NV));
+    state<<<gs, SS::THREADS, SS::BYTES, stream>>>(sa);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (ev && (e = cudaEventRecord(ev[3], stream)) != cudaSuccess) return e;
+    return cudaSuccess;
+}
+
+template <int C, int D>
+cudaError_t dispatch_dtypes(const kda_params& p, const GateParams& gp, const void* q, const void* k,
+                            const void* v, const float* g_raw, const float* b_raw, const float* A_log,
+                            const float* dt_bias, const int32_t* cu, int32_t N, int64_t T, float* pool,
+                            int64_t num_slots, const int32_t* state_idx, void* out, void* ws,
+                            cudaStream_t s, const cudaEvent_t* ev)
+{
+#define KDA_RUN(TI, TO) run_prefill<C, D, TI, TO>(p, gp, q, k, v, g_raw, b_raw, A_log, dt_bias, cu, N, T, pool, num_slots, state_idx, out, ws, s, ev)
+    if (p.io_dtype == KDA_BF16) {
+        if (p.out_dtype == KDA_BF16) return KDA_RUN(__nv_bfloat16, __nv_bfloat16);
+        return KDA_RUN(__nv_bfloat16, float);
+    }
+    if (p.out_dtype == KDA_BF16) return KDA_RUN(float, __nv_bfloat16);
+    return KDA_RUN(float, float);
+#undef KDA_RUN
+}
+
+}  // namespace
+
+bool prefill_supported(const kda_params& p)
+{
+    const bool dim = p.head_dim == 16 || p.head_dim == 32 || p.head_dim == 64 || p.head_dim == 128;
+    const bool chunk = p.chunk_size == 16 || p.chunk_size == 32 || p.chunk_size == 64;
+    const bool dt = (p.io_dtype == KDA_F32 || p.io_dtype == KDA_BF16) &&
+                    (p.out_dtype == KDA_F32 || p.out_dtype == KDA_BF16);
+    return dim && chunk && dt && p.gate_kind == KDA_GATE_PER_CHANNEL;
+}
+
+size_t prefill_workspace_bytes(const kda_params& p, int32_t num_seqs, int64_t total_tokens)
+{
+    return ws_layout(p.chunk_size, p.head_dim, p.num_heads, num_seqs, total_tokens).total_bytes;
+}
+
+cudaError_t launch_prefill(const kda_params& p, const GateParams& gp, const void* q,
+                           const void* k, const void* v, const float* g_raw, const float* b_raw,
+                           const float* A_log, const float* dt_bias, const int32_t* cu_seqlens,
+                           int32_t num_seqs, int64_t total_tokens, float* pool,
+                           int64_t num_slots, const int32_t* state_idx, void* out,
+                           void* workspace, cudaStream_t stream, const cudaEvent_t* events)
+{
+#define KDA_DIM(CC, DD)                                                                            \
+    if (p.chunk_size == CC && p.head_dim == DD)                                                    \
+        return dispatch_dtypes<CC, DD>(p, gp, q, k, v, g_raw, b_raw, A_log, dt_bias, cu_seqlens,  \
+                                       num_seqs, total_tokens, pool, num_slots, state_idx, out,    \
+                                       workspace, stream, events);
+    KDA_DIM(16, 16) KDA_DIM(16, 32) KDA_DIM(16, 64) KDA_DIM(16, 128)
+    KDA_DIM(32, 16) KDA_DIM(32, 32) KDA_DIM(32, 64) KDA_DIM(32, 128)
+    KDA_DIM(64, 16) KDA_DIM(64, 32) KDA_DIM(64, 64) KDA_DIM(64, 128)
+#undef KDA_DIM
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t prefill_read_and_clear_error(int32_t* code)
+{
+    int32_t zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_prefill_error, sizeof(int32_t));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_prefill_error, &zero, sizeof(int32_t));
+}
+
+}  // namespace kda

@@ -1,0 +1,306 @@
+// kda_recurrent.cu -- single-token decode and multi-token verify of the KDA / GDN recurrence.
+//
+// One CTA owns one (request, head) state tile S^T [D][D] fp32 (value row j, key channel c
+// contiguous, the pool's layout).  The tile is streamed from HBM once with 16-byte loads,
+// kept in registers across the request's tokens, and written once (decode: back into the pool
+// slot; verify: once per draft token into the intermediate-state buffer).
+//
+// Per token, following the five steps of "linear_attention" (zdszero.github.io), section
+// "Gated DeltaNet", with the per-channel decay of section "KDA：逐通道的遗忘门":
+//   S' = S Diag(alpha) (transposed storage: column c of S^T scaled by alpha_c)   decay
+//   v_hat_j = sum_c S'[j][c] k_c                                                 predict
+//   delta_j = beta (v_j - v_hat_j)                                                error
+//   S[j][c] = S'[j][c] + delta_j k_c                                             write
+//   o_j     = sum_c S'[j][c] q_c + delta_j (q . k)  ( = q S_t )                  read
+// The readout uses the decomposition of "ReplaySSM -- buffered output-only decode", section
+// 3.12, so both row reductions (k . S'_j and q . S'_j) are taken in one pass.
+//
+// Thread mapping: a warp handles 16 rows; a row is split over LPR lanes, each lane holding CPL
+// consecutive-in-pattern columns (float4 groups 4*li + 4*LPR*j), so every load instruction of a
+// warp reads whole 128-byte row segments.  Row sums are reduced with log2(LPR) xor-shuffles.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+__device__ int32_t g_recurrent_error = 0;
+
+__device__ __forceinline__ void record_error(int32_t code) { atomicCAS(&g_recurrent_error, 0, code); }
+
+struct RecArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g_raw;
+    const float* b_raw;
+    const float* A_log;
+    const float* dt_bias;
+    const float* pool_in;
+    float* pool_out;    // decode: == pool_in (in place); verify: unused
+    float* inter;       // verify: [batch][t_draft][H][D][D]; decode: unused
+    const int32_t* state_idx;
+    void* out;
+    int64_t num_slots;
+    int H;
+    int t_draft;
+    GateParams gp;
+};
+
+template <int D>
+struct RecShape {
+    static constexpr int NWARPS = D >= 32 ? D / 16 : 1;
+    static constexpr int THREADS = NWARPS * 32;
+    static constexpr int CPL = D >= 32 ? 16 : 8;   // columns per lane
+    static constexpr int LPR = D / CPL;             // lanes per row
+    static constexpr int RPS = 32 / LPR;            // rows per warp step
+    static constexpr int ROWS_PER_WARP = D / NWARPS;
+    static constexpr int STEPS = ROWS_PER_WARP / RPS;
+    static constexpr int NV4 = CPL / 4;             // float4 groups per lane and row
+    static_assert(ROWS_PER_WARP % RPS == 0, "row split");
+    static_assert(NWARPS * ROWS_PER_WARP == D, "rows");
+};
+
+// GATE: KDA_GATE_PER_CHANNEL or KDA_GATE_PER_HEAD.  VERIFY: write every intermediate state to
+// `inter` and leave the pool untouched; otherwise update the pool slot in place (t_draft = 1).
+template <int D, int GATE, bool VERIFY, typename TIn, typename TOut>
+__global__ void __launch_bounds__(RecShape<D>::THREADS, (D >= 128 ? 2 : 4))
+recurrent_kernel(const RecArgs a)
+{
+    using Sh = RecShape<D>;
+    constexpr int NWARPS = Sh::NWARPS, CPL = Sh::CPL, LPR = Sh::LPR, RPS = Sh::RPS;
+    constexpr int STEPS = Sh::STEPS, NV4 = Sh::NV4;
+
+    __shared__ float s_k[D];
+    __shared__ float s_q[D];
+    __shared__ float s_alpha[D];
+    __shared__ float s_red[3][NWARPS];
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int H = a.H;
+    const int64_t bh = blockIdx.x;
+    const int64_t b = bh / H;
+    const int h = (int)(bh - b * H);
+    const int T = VERIFY ? a.t_draft : 1;
+
+    int64_t slot = a.state_idx[b];
+    if (slot >= a.num_slots) {
+        if (tid == 0) record_error(kDevErrStateIndex);
+        slot = -1;
+    }
+    TOut* out = reinterpret_cast<TOut*>(a.out);
+    if (slot < 0) {  // padding row: zero outputs, no state traffic
+        for (int t = 0; t < T; ++t) {
+            const int64_t tok = b * T + t;
+            for (int j = tid; j < D; j += Sh::THREADS) out[(tok * H + h) * D + j] = from_f32<TOut>(0.f);
+        }
+        return;
+    }
+
+    const int row_in_step = lane / LPR;
+    const int li = lane % LPR;
+    const size_t tile = ((size_t)slot * H + h) * (size_t)D * D;
+
+    // Issue every state load of this thread first; the gate/norm prologue overlaps their latency.
+    float4 st[STEPS][NV4];
+#pragma unroll
+    for (int s = 0; s < STEPS; ++s) {
+        const int row = warp * Sh::ROWS_PER_WARP + s * RPS + row_in_step;
+        const float4* src = reinterpret_cast<const float4*>(a.pool_in + tile + (size_t)row * D);
+#pragma unroll
+        for (int j = 0; j < NV4; ++j) st[s][j] = __ldcs(src + li + LPR * j);
+    }
+
+    const TIn* qp = reinterpret_cast<const TIn*>(a.q);
+    const TIn* kp = reinterpret_cast<const TIn*>(a.k);
+    const TIn* vp = reinterpret_cast<const TIn*>(a.v);
+    const float rate = expf(a.A_log[h]);
+
+    for (int t = 0; t < T; ++t) {
+        const int64_t tok = b * T + t;
+        const size_t rowbase = ((size_t)tok * H + h) * D;
+
+        // ---- prologue: L2 norms, q.k, gate and beta for this token --------------------------
+        float kc = 0.f, qc = 0.f;
+        if (tid < D) {
+            kc = to_f32(kp[rowbase + tid]);
+            qc = to_f32(qp[rowbase + tid]);
+            if (GATE == KDA_GATE_PER_CHANNEL) {
+                const float x = a.g_raw[rowbase + tid] + (a.dt_bias ? a.dt_bias[(size_t)h * D + tid] : 0.f);
+                s_alpha[tid] = expf(gate_log_decay(x, rate, a.gp));
+            }
+        }
+        float kk = kc * kc, qq = qc * qc, kq = kc * qc;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            kk += __shfl_xor_sync(0xffffffffu, kk, off);
+            qq += __shfl_xor_sync(0xffffffffu, qq, off);
+            kq += __shfl_xor_sync(0xffffffffu, kq, off);
+        }
+        if (lane == 0) {
+            s_red[0][warp] = kk;
+            s_red[1][warp] = qq;
+            s_red[2][warp] = kq;
+        }
+        __syncthreads();
+        kk = 0.f; qq = 0.f; kq = 0.f;
+#pragma unroll
+        for (int w = 0; w < NWARPS; ++w) {
+            kk += s_red[0][w];
+            qq += s_red[1][w];
+            kq += s_red[2][w];
+        }
+        const float rk = 1.0f / sqrtf(kk + a.gp.l2_eps);
+        const float rq = a.gp.scale / sqrtf(qq + a.gp.l2_eps);
+        const float qk = kq * rk * rq;
+        const float beta = sigmoid_f32(a.b_raw[(size_t)tok * H + h]);
+        float alpha_h = 1.f;
+        if (GATE == KDA_GATE_PER_HEAD) {
+            const float x = a.g_raw[(size_t)tok * H + h] + (a.dt_bias ? a.dt_bias[h] : 0.f);
+            alpha_h = expf(gate_log_decay(x, rate, a.gp));
+        }
+        if (tid < D) {
+            s_k[tid] = kc * rk;
+            s_q[tid] = qc * rq;
+        }
+        __syncthreads();
+
+        // ---- per-lane column constants --------------------------------------------------------
+        float kh[CPL], qh[CPL], al[CPL];
+#pragma unroll
+        for (int j = 0; j < NV4; ++j) {
+            const int c = 4 * (li + LPR * j);
+            const float4 k4 = *reinterpret_cast<const float4*>(&s_k[c]);
+            const float4 q4 = *reinterpret_cast<const float4*>(&s_q[c]);
+            kh[4 * j + 0] = k4.x; kh[4 * j + 1] = k4.y; kh[4 * j + 2] = k4.z; kh[4 * j + 3] = k4.w;
+            qh[4 * j + 0] = q4.x; qh[4 * j + 1] = q4.y; qh[4 * j + 2] = q4.z; qh[4 * j + 3] = q4.w;
+            if (GATE == KDA_GATE_PER_CHANNEL) {
+                const float4 a4 = *reinterpret_cast<const float4*>(&s_alpha[c]);
+                al[4 * j + 0] = a4.x; al[4 * j + 1] = a4.y; al[4 * j + 2] = a4.z; al[4 * j + 3] = a4.w;
+            } else {
+                al[4 * j + 0] = al[4 * j + 1] = al[4 * j + 2] = al[4 * j + 3] = alpha_h;
+            }
+        }
+
+        // ---- rows: decay, predict, error, write, read -----------------------------------------
+#pragma unroll
+        for (int s = 0; s < STEPS; ++s) {
+            const int row = warp * Sh::ROWS_PER_WARP + s * RPS + row_in_step;
+            const float vj = to_f32(vp[rowbase + row]);
+            float pk = 0.f, pq = 0.f;
+#pragma unroll
+            for (int j = 0; j < NV4; ++j) {
+                float4& e = st[s][j];
+                e.x *= al[4 * j + 0]; e.y *= al[4 * j + 1]; e.z *= al[4 * j + 2]; e.w *= al[4 * j + 3];
+                pk = fmaf(e.x, kh[4 * j + 0], pk); pk = fmaf(e.y, kh[4 * j + 1], pk);
+                pk = fmaf(e.z, kh[4 * j + 2], pk); pk = fmaf(e.w, kh[4 * j + 3], pk);
+                pq = fmaf(e.x, qh[4 * j + 0], pq); pq = fmaf(e.y, qh[4 * j + 1], pq);
+                pq = fmaf(e.z, qh[4 * j + 2], pq); pq = fmaf(e.w, qh[4 * j + 3], pq);
+            }
+#pragma unroll
+            for (int off = LPR / 2; off > 0; off >>= 1) {
+                pk += __shfl_xor_sync(0xffffffffu, pk, off);
+                pq += __shfl_xor_sync(0xffffffffu, pq, off);
+            }
+            const float delta = beta * (vj - pk);
+            const float o = fmaf(delta, qk, pq);
+#pragma unroll
+            for (int j = 0; j < NV4; ++j) {
+                float4& e = st[s][j];
+                e.x = fmaf(delta, kh[4 * j + 0], e.x); e.y = fmaf(delta, kh[4 * j + 1], e.y);
+                e.z = fmaf(delta, kh[4 * j + 2], e.z); e.w = fmaf(delta, kh[4 * j + 3], e.w);
+            }
+            if (li == 0) out[rowbase + row] = from_f32<TOut>(o);
+            float* dst;
+            if (VERIFY) {
+                dst = a.inter + ((((size_t)b * T + t) * H + h) * (size_t)D + row) * D;
+            } else {
+                dst = a.pool_out + tile + (size_t)row * D;
+            }
+            float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+            for (int j = 0; j < NV4; ++j) __stcs(d4 + li + LPR * j, st[s][j]);
+        }
+        if (VERIFY) __syncthreads();  // the next token rewrites the shared column constants
+    }
+}
+
+template <int D, int GATE, bool VERIFY, typename TIn, typename TOut>
+cudaError_t launch_t(const RecArgs& a, int64_t batch, cudaStream_t stream)
+{
+    const int64_t blocks = batch * a.H;
+    if (blocks <= 0) return cudaSuccess;
+    recurrent_kernel<D, GATE, VERIFY, TIn, TOut><<<(unsigned)blocks, RecShape<D>::THREADS, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <int D, int GATE, bool VERIFY>
+cudaError_t dispatch_dtypes(const kda_params& p, const RecArgs& a, int64_t batch, cudaStream_t s)
+{
+    if (p.io_dtype == KDA_BF16) {
+        if (p.out_dtype == KDA_BF16) return launch_t<D, GATE, VERIFY, __nv_bfloat16, __nv_bfloat16>(a, batch, s);
+        return launch_t<D, GATE, VERIFY, __nv_bfloat16, float>(a, batch, s);
+    }
+    if (p.out_dtype == KDA_BF16) return launch_t<D, GATE, VERIFY, float, __nv_bfloat16>(a, batch, s);
+    return launch_t<D, GATE, VERIFY, float, float>(a, batch, s);
+}
+
+template <int D, bool VERIFY>
+cudaError_t dispatch_gate(const kda_params& p, const RecArgs& a, int64_t batch, cudaStream_t s)
+{
+    if (p.gate_kind == KDA_GATE_PER_HEAD) return dispatch_dtypes<D, KDA_GATE_PER_HEAD, VERIFY>(p, a, batch, s);
+    return dispatch_dtypes<D, KDA_GATE_PER_CHANNEL, VERIFY>(p, a, batch, s);
+}
+
+template <bool VERIFY>
+cudaError_t dispatch_dim(const kda_params& p, const RecArgs& a, int64_t batch, cudaStream_t s)
+{
+    switch (p.head_dim) {
+    case 16: return dispatch_gate<16, VERIFY>(p, a, batch, s);
+    case 32: return dispatch_gate<32, VERIFY>(p, a, batch, s);
+    case 64: return dispatch_gate<64, VERIFY>(p, a, batch, s);
+    case 128: return dispatch_gate<128, VERIFY>(p, a, batch, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+bool recurrent_supported(const kda_params& p)
+{
+    const bool dim = p.head_dim == 16 || p.head_dim == 32 || p.head_dim == 64 || p.head_dim == 128;
+    const bool dt = (p.io_dtype == KDA_F32 || p.io_dtype == KDA_BF16) &&
+                    (p.out_dtype == KDA_F32 || p.out_dtype == KDA_BF16);
+    const bool gate = p.gate_kind == KDA_GATE_PER_CHANNEL || p.gate_kind == KDA_GATE_PER_HEAD;
+    return dim && dt && gate;
+}
+
+cudaError_t launch_recurrent(const kda_params& p, const GateParams& gp, const void* q,
+                             const void* k, const void* v, const float* g_raw,
+                             const float* b_raw, const float* A_log, const float* dt_bias,
+                             int32_t batch, int32_t t_draft, const float* pool_in,
+                             float* pool_out, float* inter, int64_t num_slots,
+                             const int32_t* state_idx, void* out, cudaStream_t stream)
+{
+    RecArgs a;
+    a.q = q; a.k = k; a.v = v; a.g_raw = g_raw; a.b_raw = b_raw; a.A_log = A_log; a.dt_bias = dt_bias;
+    a.pool_in = pool_in; a.pool_out = pool_out; a.inter = inter; a.state_idx = state_idx; a.out = out;
+    a.num_slots = num_slots; a.H = p.num_heads; a.t_draft = t_draft; a.gp = gp;
+    if (inter != nullptr) return dispatch_dim<true>(p, a, batch, stream);
+    return dispatch_dim<false>(p, a, batch, stream);
+}
+
+cudaError_t recurrent_read_and_clear_error(int32_t* code)
+{
+    int32_t zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_recurrent_error, sizeof(int32_t));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_recurrent_error, &zero, sizeof(int32_t));
+}
+
+}  // namespace kda

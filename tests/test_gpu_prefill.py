@@ -1,0 +1,177 @@
+"""GPU parity of kda_chunk_prefill against the fp64 oracle through the C ABI: the tiny fp32
+workload, edge shapes (single tokens, chunk-boundary lengths, ragged varlen, padding rows,
+empty sequences), the full varlen workload, the long prefill split into 32 calls carrying the
+state (sampled heads), and the mode invariances (prefill then decode equals one prefill;
+chunked calls equal one call; packed varlen equals separate calls)."""
+import numpy as np
+import pytest
+import torch
+
+import kda_gated_delta_gb300 as kda
+from kda_gated_delta_gb300 import workloads
+from helpers import np64, oracle_run, rel_err, tol_for
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def run_prefill(inp, chunk, out_dtype=torch.float32, pool=None, lower_bound=None):
+    d = workloads.to_device(inp, DEV)
+    pool = d["pool"].clone() if pool is None else pool
+    out = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g_raw"], d["b_raw"], d["A_log"], d["dt_bias"],
+                            d["cu_seqlens"], pool, d["state_idx"], chunk_size=chunk, out_dtype=out_dtype,
+                            lower_bound=lower_bound)
+    torch.cuda.synchronize()
+    assert kda.check_device_errors() == 0
+    return out, pool
+
+
+def check(inp, H, D, chunk, io, out_dtype=torch.float32, lower_bound=None):
+    out, pool = run_prefill(inp, chunk, out_dtype=out_dtype, lower_bound=lower_bound)
+    o_ref, p_ref, _ = oracle_run(inp, H, D, lower_bound=lower_bound)
+    e_o = rel_err(np64(out), o_ref)
+    e_s = rel_err(np64(pool), p_ref)
+    assert e_o <= tol_for(io, out_dtype), e_o
+    assert e_s <= tol_for(io, torch.float32), e_s
+    return out, pool, e_o, e_s
+
+
+def test_tiny_fp32_workload():
+    """1 sequence T = 64, H = 2, d = 16, chunk 16, fp32, S0 = 0: max relative error <= 1e-5."""
+    w = workloads.workload(0)
+    inp = workloads.workload_inputs(0)
+    check(inp, w.num_heads, w.head_dim, w.chunk_size, torch.float32)
+
+
+@pytest.mark.parametrize("lengths", [[1], [8], [63], [64], [65], [128], [5, 17, 1, 41], [32] * 4, [200, 0, 7]])
+def test_edge_shapes_bf16(lengths):
+    H, D = 4, 128
+    inp = workloads.make_inputs(lengths, H, D, torch.bfloat16, pool_slots=9, pool_std=0.05, seed=sum(lengths),
+                                dt_bias_std=0.5)
+    check(inp, H, D, 64, torch.bfloat16)
+
+
+@pytest.mark.parametrize("C,D", [(16, 16), (16, 32), (32, 64), (64, 64), (16, 128), (32, 128), (64, 32)])
+@pytest.mark.parametrize("io", [torch.float32, torch.bfloat16])
+def test_chunk_and_dim_grid(C, D, io):
+    H = 3
+    inp = workloads.make_inputs([37, 130, 64], H, D, io, pool_slots=5, pool_std=0.1, seed=C * 1000 + D,
+                                dt_bias_std=0.3)
+    check(inp, H, D, C, io)
+
+
+def test_padding_rows_and_untouched_slots():
+    H, D = 2, 64
+    inp = workloads.make_inputs([20, 70, 3], H, D, torch.float32, pool_slots=6, pool_std=0.1, seed=3,
+                                padding_rows=(1,))
+    out, pool, _, _ = check(inp, H, D, 32, torch.float32)
+    cu = inp["cu_seqlens"].tolist()
+    assert np.all(np64(out)[cu[1]:cu[2]] == 0.0)
+    used = set(inp["state_idx"].tolist())
+    for s in range(6):
+        if s not in used:
+            assert torch.equal(pool[s].cpu(), inp["pool"][s])
+
+
+def test_mild_and_strong_gates_fp32():
+    """Gates from nearly no decay (g ~ -1e-3) to decays that underflow fp32 within a few tokens."""
+    H, D = 2, 64
+    for g_mean, seed in ((-8.0, 1), (4.0, 2)):
+        inp = workloads.make_inputs([150, 90], H, D, torch.float32, pool_slots=3, pool_std=0.1, seed=seed,
+                                    g_mean=g_mean, g_std=2.0)
+        check(inp, H, D, 64, torch.float32)
+
+
+def test_safe_gate_and_bf16_output():
+    H, D = 4, 128
+    inp = workloads.make_inputs([300, 45], H, D, torch.bfloat16, pool_slots=4, pool_std=0.05, seed=12,
+                                dt_bias_std=3.0)
+    check(inp, H, D, 64, torch.bfloat16, out_dtype=torch.bfloat16, lower_bound=-5.0)
+
+
+def test_varlen_workload_full():
+    """8 sequences with lengths U[512, 4096], H = 32, d = 128, bf16, chunk 64, 512-slot pool."""
+    inp = workloads.workload_inputs(1)
+    out, pool = run_prefill(inp, 64, out_dtype=torch.float32)
+    o_ref, p_ref, _ = oracle_run(inp, 32, 128)
+    assert rel_err(np64(out), o_ref) <= tol_for(torch.bfloat16, torch.float32)
+    assert rel_err(np64(pool), p_ref) <= tol_for(torch.bfloat16, torch.float32)
+    out_b, _ = run_prefill(inp, 64, out_dtype=torch.bfloat16)
+    assert rel_err(np64(out_b), o_ref) <= tol_for(torch.bfloat16, torch.bfloat16)
+
+
+def test_long_chunked_prefill_sampled_heads():
+    """1 sequence of 131072 tokens as 32 successive 4096-token calls carrying the state in one
+    slot; heads 0 and 19 are compared against the oracle over the whole sequence."""
+    w = workloads.workload(3)
+    inp = workloads.workload_inputs(3)
+    d = workloads.to_device(inp, DEV)
+    pool = d["pool"].clone()
+    T, per = 131072, 4096
+    out = torch.empty(T, 32, 128, device=DEV, dtype=torch.float32)
+    cu = torch.tensor([0, per], dtype=torch.int32, device=DEV)
+    ws = torch.empty(kda.prefill_workspace_size(kda.make_params(32, 128), 1, per), dtype=torch.uint8, device=DEV)
+    for c in range(w.calls):
+        s = slice(c * per, (c + 1) * per)
+        kda.chunk_prefill(d["q"][s], d["k"][s], d["v"][s], d["g_raw"][s], d["b_raw"][s], d["A_log"],
+                          d["dt_bias"], cu, pool, d["state_idx"], out[s], out_dtype=torch.float32,
+                          workspace=ws)
+    torch.cuda.synchronize()
+    heads = [0, 19]
+    o_ref, p_ref, _ = oracle_run(inp, 32, 128, heads=heads)
+    assert rel_err(np64(out[:, heads]), o_ref[:, heads]) <= tol_for(torch.bfloat16, torch.float32)
+    assert rel_err(np64(pool[:, heads]), p_ref[:, heads]) <= tol_for(torch.bfloat16, torch.float32)
+
+
+def test_prefill_then_decode_equals_one_prefill():
+    """prefill(seq[:T]) == prefill(seq[:T-k]) followed by k single-token decodes (k = 8)."""
+    H, D, T, k = 4, 128, 200, 8
+    inp = workloads.make_inputs([T], H, D, torch.float32, pool_slots=2, pool_std=0.1, seed=44)
+    out_full, pool_full = run_prefill(inp, 64)
+    d = workloads.to_device(inp, DEV)
+    pool = d["pool"].clone()
+    head = {n: d[n][:T - k].contiguous() for n in ("q", "k", "v", "g_raw", "b_raw")}
+    cu = torch.tensor([0, T - k], dtype=torch.int32, device=DEV)
+    o1 = kda.chunk_prefill(head["q"], head["k"], head["v"], head["g_raw"], head["b_raw"], d["A_log"],
+                           d["dt_bias"], cu, pool, d["state_idx"], chunk_size=64, out_dtype=torch.float32)
+    outs = [o1]
+    for t in range(T - k, T):
+        s = slice(t, t + 1)
+        outs.append(kda.recurrent_decode(d["q"][s], d["k"][s], d["v"][s], d["g_raw"][s], d["b_raw"][s],
+                                         d["A_log"], d["dt_bias"], pool, d["state_idx"],
+                                         out_dtype=torch.float32))
+    torch.cuda.synchronize()
+    scale = out_full.abs().max().item()
+    assert (torch.cat(outs) - out_full).abs().max().item() <= 1e-5 * scale
+    assert (pool - pool_full).abs().max().item() <= 1e-5 * pool_full.abs().max().item()
+
+
+def test_packed_varlen_equals_separate_calls():
+    H, D = 4, 64
+    lengths = [33, 100, 1, 64]
+    inp = workloads.make_inputs(lengths, H, D, torch.float32, pool_slots=8, pool_std=0.1, seed=55)
+    out_all, pool_all = run_prefill(inp, 32)
+    d = workloads.to_device(inp, DEV)
+    cu = inp["cu_seqlens"].tolist()
+    for i in range(len(lengths)):
+        pool = d["pool"].clone()
+        s = slice(cu[i], cu[i + 1])
+        o = kda.chunk_prefill(d["q"][s].contiguous(), d["k"][s].contiguous(), d["v"][s].contiguous(),
+                              d["g_raw"][s].contiguous(), d["b_raw"][s].contiguous(), d["A_log"], d["dt_bias"],
+                              torch.tensor([0, lengths[i]], dtype=torch.int32, device=DEV), pool,
+                              d["state_idx"][i:i + 1].contiguous(), chunk_size=32, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert torch.equal(o, out_all[s])
+        slot = int(inp["state_idx"][i])
+        assert torch.equal(pool[slot], pool_all[slot])
+
+
+def test_malformed_cu_seqlens_is_recorded_not_faulting():
+    H, D = 2, 32
+    inp = workloads.make_inputs([10, 10], H, D, torch.float32, pool_slots=2, seed=6)
+    inp["cu_seqlens"] = torch.tensor([0, 15, 12], dtype=torch.int32)   # decreasing, ends short of T
+    d = workloads.to_device(inp, DEV)
+    kda.check_device_errors()
+    kda.chunk_prefill(d["q"], d["k"], d["v"], d["g_raw"], d["b_raw"], d["A_log"], d["dt_bias"],
+                      d["cu_seqlens"], d["pool"].clone(), d["state_idx"], chunk_size=16, out_dtype=torch.float32)
+    assert kda.check_device_errors() == 2
