@@ -58,7 +58,8 @@ typedef enum kda_status {
     KDA_ERR_MISALIGNED = -3,   /* a tensor pointer is not 16-byte aligned */
     KDA_ERR_WORKSPACE = -4,    /* workspace NULL, too small or not 256-byte aligned */
     KDA_ERR_CUDA = -5,         /* a CUDA runtime call or kernel launch failed */
-    KDA_ERR_DEVICE_CHECK = -6  /* kda_check_device_errors found a recorded argument error */
+    KDA_ERR_DEVICE_CHECK = -6, /* kda_check_device_errors found a recorded argument error */
+    KDA_ERR_SCRATCH_LIMIT = -7 /* the problem needs more scratch than KDA_STATIC_SCRATCH_BYTES */
 } kda_status;
 
 typedef enum kda_dtype { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -169,6 +170,42 @@ int32_t kda_recurrent_verify(const kda_params* p,
                              const float* state_pool, int64_t num_slots, const int32_t* state_idx,
                              float* inter_states, void* out,
                              kda_stream_t stream);
+
+/*
+ * kda_chunk_prefill for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this entry point; it exists for the library's users.
+ *
+ * Who needs it: code that may not call cudaMalloc or any allocator, for example a plugin inside
+ * a serving process that has already handed all device memory to its own pools, a runtime with
+ * no binding to a CUDA allocator, or a latency-critical loop that must not risk the device-wide
+ * synchronisation a cudaMalloc can cause.  Such a caller cannot provide the workspace that
+ * kda_chunk_prefill asks for.
+ *
+ * What it does: exactly the work of kda_chunk_prefill, with the same arguments minus the
+ * workspace.  Its scratch is a fixed array of KDA_STATIC_SCRATCH_BYTES compiled into the library;
+ * every GPU that loads the library holds that much device memory for it until the process exits.
+ * The call allocates nothing.  A problem whose kda_chunk_prefill_workspace_size(...) exceeds
+ * KDA_STATIC_SCRATCH_BYTES is rejected with KDA_ERR_SCRATCH_LIMIT before any work is enqueued
+ * (with H = 32, head_dim = 128, chunk 64 the array covers ceil(T / 64) + num_seqs <= 56 chunks,
+ * about 3,000 tokens per call).
+ *
+ * The first call on each device looks up the device address of the array (this can load the
+ * library's device code on that device); make that first call outside any stream capture.
+ * All calls share the one array and it keeps whatever the last call left in it (nothing in it
+ * needs to start at zero).  Calls whose kernels overlap on the GPU, on different streams or
+ * from different host threads, race on the array and produce garbage: order them.
+ */
+#define KDA_STATIC_SCRATCH_BYTES ((size_t)256 << 20)
+int32_t kda_chunk_prefill_static_scratch(const kda_params* p,
+                                         const void* q, const void* k, const void* v,
+                                         const float* g_raw, const float* b_raw,
+                                         const float* A_log, const float* dt_bias,
+                                         const int32_t* cu_seqlens, int32_t num_seqs,
+                                         int64_t total_tokens,
+                                         float* state_pool, int64_t num_slots,
+                                         const int32_t* state_idx,
+                                         void* out,
+                                         kda_stream_t stream);
 
 /*
  * Synchronise `stream`, then read and clear the device error word that the kernels set when

@@ -20,7 +20,7 @@ GATE_PER_CHANNEL, GATE_PER_HEAD = 0, 1
 
 _STATUS = {
     0: "KDA_OK", -1: "KDA_ERR_INVALID_ARG", -2: "KDA_ERR_UNSUPPORTED", -3: "KDA_ERR_MISALIGNED",
-    -4: "KDA_ERR_WORKSPACE", -5: "KDA_ERR_CUDA", -6: "KDA_ERR_DEVICE_CHECK",
+    -4: "KDA_ERR_WORKSPACE", -5: "KDA_ERR_CUDA", -6: "KDA_ERR_DEVICE_CHECK", -7: "KDA_ERR_SCRATCH_LIMIT",
 }
 
 

@@ -73,6 +73,7 @@ const char* kda_status_string(int32_t status)
     case KDA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
     case KDA_ERR_CUDA: return "CUDA runtime error";
     case KDA_ERR_DEVICE_CHECK: return "a kernel recorded an invalid state_idx or cu_seqlens";
+    case KDA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the library's fixed scratch array holds";
     default: return "unknown status";
     }
 }
