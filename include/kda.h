@@ -209,8 +209,9 @@ int32_t kda_chunk_prefill_static_scratch(const kda_params* p,
 
 /*
  * Synchronise `stream`, then read and clear the device error word that the kernels set when
- * they meet an out-of-range state_idx or a malformed cu_seqlens.  *code receives the first
- * recorded code (0 when none) for the current device.  Returns KDA_OK when no error was
+ * they meet an out-of-range state_idx (code 1), a malformed cu_seqlens (code 2) or a bounded
+ * wait inside a kernel that gave up (code 3; that call's results are invalid).  *code receives
+ * the first recorded code (0 when none) for the current device.  Returns KDA_OK when no error was
  * recorded, KDA_ERR_DEVICE_CHECK when one was, KDA_ERR_CUDA when the synchronisation failed.
  */
 int32_t kda_check_device_errors(kda_stream_t stream, int32_t* code);

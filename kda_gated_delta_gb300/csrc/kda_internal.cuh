@@ -15,6 +15,7 @@ enum DeviceError : int32_t {
     kDevErrNone = 0,
     kDevErrStateIndex = 1,   // state_idx[i] >= num_slots
     kDevErrSeqlens = 2,      // cu_seqlens not non-decreasing within [0, T]
+    kDevErrTimeout = 3,      // a bounded wait inside a kernel gave up (the call's results are invalid)
 };
 
 // Scalar parameters every kernel needs, resolved on the host from kda_params.
