@@ -58,7 +58,7 @@ struct TcRec {
 };
 
 // ---- workspace layout ----------------------------------------------------------------------
-// [chunk table: 3 * max_chunks + (N + 1) int32, padded to 256 B]
+// [chunk table: 3 * max_chunks + (N + 1) + N int32, padded to 256 B]
 // [per (chunk, head): W C*D | Qbar C*D | Ktil C*D | U C*D | P C*C | gL D  floats, padded to 64]
 struct WsLayout {
     int64_t max_chunks;
@@ -73,7 +73,7 @@ WsLayout ws_layout(int C, int D, int H, int32_t N, int64_t T)
 {
     WsLayout w;
     w.max_chunks = (T + C - 1) / C + N;
-    w.table_bytes = round_up(sizeof(int32_t) * (size_t)(3 * w.max_chunks + N + 1), 256);
+    w.table_bytes = round_up(sizeof(int32_t) * (size_t)(3 * w.max_chunks + 2 * (int64_t)N + 1), 256);
     w.per_chunk_head = round_up((size_t)4 * C * D + (size_t)C * C + D, 64);
     w.total_bytes = w.table_bytes + sizeof(float) * w.per_chunk_head * (size_t)w.max_chunks * H;
     return w;
@@ -83,10 +83,14 @@ WsLayout ws_layout(int C, int D, int H, int32_t N, int64_t T)
 // One CTA of 1024 threads.  chunk i of the packed batch covers tokens
 // chunk_start[i] .. chunk_start[i] + chunk_len[i] - 1 of sequence chunk_seq[i]; the chunks of
 // sequence s are seq_off[s] .. seq_off[s+1]-1 and seq_off[N] is the number of chunks.
+// seq_order lists the sequences by decreasing chunk count (ties by index; identity when
+// N > 4096), so that the state pass starts its longest serial chains first.
+constexpr int32_t kMaxSortedSeqs = 4096;
 __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* __restrict__ cu, int32_t N, int64_t T,
                                                            int C, int64_t max_chunks,
                                                            int32_t* chunk_seq, int32_t* chunk_start,
-                                                           int32_t* chunk_len, int32_t* seq_off)
+                                                           int32_t* chunk_len, int32_t* seq_off,
+                                                           int32_t* seq_order)
 {
     __shared__ int32_t s_warp[32];
     __shared__ int32_t s_base;
@@ -148,6 +152,20 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* __rest
         __syncthreads();
     }
     if (tid == 0) seq_off[N] = s_base;
+    __syncthreads();
+    for (int32_t i = tid; i < N; i += blockDim.x) {
+        if (N > kMaxSortedSeqs) {
+            seq_order[i] = i;
+            continue;
+        }
+        const int32_t ni = seq_off[i + 1] - seq_off[i];
+        int32_t rank = 0;
+        for (int32_t j = 0; j < N; ++j) {
+            const int32_t nj = seq_off[j + 1] - seq_off[j];
+            rank += (nj > ni) || (nj == ni && j < i);
+        }
+        seq_order[rank] = i;
+    }
 }
 
 // ---- intra-chunk kernel ----------------------------------------------------------------------
@@ -476,6 +494,7 @@ __global__ void __launch_bounds__(IntraShape<C, D>::THREADS, 1) chunk_intra_kern
 
 // ---- inter-chunk state pass ----------------------------------------------------------------------
 struct StateArgs {
+    const int32_t* seq_order;   // sequences by decreasing chunk count (tensor-core pass)
     const int32_t* chunk_start;
     const int32_t* chunk_len;
     const int32_t* seq_off;
@@ -652,26 +671,33 @@ __global__ void __launch_bounds__(256, 1) chunk_state_kernel(const StateArgs a)
 // One CTA of 128 threads per (sequence, head); thread v owns value row v: its row of S^T lives in
 // registers (fp32), and it is TMEM lane v.  Per chunk, in the transposed ("value-major") form so
 // that every MMA has M = 128 rows = the 128 value rows:
-//   (a) Dd   = S^T W^T                   A = tf32 copy of S^T in TMEM, B = W image       (N = 64)
-//   (b) Do   = S^T Qbar^T                A = S^T,                      B = Qbar image    (N = 64)
+//   (a)  Dd   = S^T W^T                  A = tf32 copy of S^T in TMEM, B = W image       (N = 64)
 //   threads: Delta^T = U^T - Dd -> tf32 copy in TMEM;  S^T <- S^T Diag(e^{G_L}) in registers
-//   (b2) Do += Delta^T P^T               A = Delta^T in TMEM,          B = P image       (N = 64)
-//   (c) Dc   = Delta^T Ktil              A = Delta^T,                  B = Ktil^T image  (N = 128)
+//   (b2) Do   = Delta^T P^T              A = Delta^T in TMEM,          B = P image       (N = 64)
+//   (c)  Dc   = Delta^T Ktil             A = Delta^T,                  B = Ktil^T image  (N = 128)
+//   (b)  Do  += S^T Qbar^T               A = S^T,                      B = Qbar image    (N = 64)
 //   threads: S^T += Dc (fp32), refresh the tf32 copy; O^T = Do -> out
-// Operand images arrive by bulk async copy from the record; each buffer is refilled for the next
-// chunk as soon as the MMAs that read it have completed.  All waits are bounded.
+// (a) and the Delta step are the serial chain; (b) is issued last so that Qbar has the longest
+// lead time.  Operand images arrive by bulk async copy from the record: W and U/gL are
+// double-buffered (loaded two chunks ahead), Qbar, P and Ktil^T are reloaded as soon as the
+// chunk's MMAs retire.  All waits are bounded.
 constexpr uint32_t kWaitPolls = 1u << 24;
 
+// shared memory: the record image (one buffer set) followed by the second W and U/gL buffers
+constexpr uint32_t kSmW1 = TcRec::BYTES;
+constexpr uint32_t kSmUG1 = kSmW1 + 32768;
+constexpr uint32_t kUGBytes = 32768 + 512;
+constexpr uint32_t kSmBars = kSmUG1 + kUGBytes;
 struct TcBars {
-    uint64_t w, kt, ug, qb, p;  // operand buffers filled (tx bytes)
-    uint64_t mma_a;             // (a) complete
-    uint64_t mma_c;             // (a), (b), (b2), (c) complete
-    uint64_t drain;             // used once, to drain the tensor core after a failed wait
+    uint64_t w[2], ug[2], kt, qb, p;  // operand buffers filled (tx bytes)
+    uint64_t mma_a;                   // (a) complete
+    uint64_t mma_c;                   // (a), (b2), (c), (b) complete
+    uint64_t drain;                   // used once, to drain the tensor core after a failed wait
 };
-constexpr size_t kTcSmemBytes = TcRec::BYTES + 256;
+constexpr size_t kTcSmemBytes = kSmBars + 256;
+static_assert(kTcSmemBytes <= 232448, "state-pass shared memory");
 
-// TMEM column map (512 columns allocated)
-// (each accumulator starts at a multiple of its own width)
+// TMEM column map (512 columns allocated; each accumulator starts at a multiple of its width)
 constexpr uint32_t kT_SOP = 0;     // tf32 S^T        (128 cols, A operand)
 constexpr uint32_t kT_SC = 128;    // Delta^T Ktil    (128, accumulator)
 constexpr uint32_t kT_DD = 256;    // S^T W^T         (64, accumulator)
@@ -684,14 +710,16 @@ __global__ void __launch_bounds__(128, 1) chunk_state_tc_kernel(const StateArgs 
     constexpr int C = TcRec::C, D = TcRec::D;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = smem_raw;
-    TcBars* bars = reinterpret_cast<TcBars*>(sm + TcRec::BYTES);
-    uint32_t* s_taddr = reinterpret_cast<uint32_t*>(sm + TcRec::BYTES + sizeof(TcBars));
-    volatile int* s_abort = reinterpret_cast<volatile int*>(sm + TcRec::BYTES + sizeof(TcBars) + 16);
+    TcBars* bars = reinterpret_cast<TcBars*>(sm + kSmBars);
+    uint32_t* s_taddr = reinterpret_cast<uint32_t*>(sm + kSmBars + sizeof(TcBars));
+    volatile int* s_abort = reinterpret_cast<volatile int*>(sm + kSmBars + sizeof(TcBars) + 16);
 
-    const int seq = blockIdx.x;
-    const int h = blockIdx.y;
-    const int tid = threadIdx.x, warp = tid >> 5;
+    // longest sequences first: CTA x -> (rank, head), rank -> sequence through seq_order
     const int H = a.H;
+    const int rank = blockIdx.x / H;
+    const int h = blockIdx.x - rank * H;
+    const int seq = a.seq_order[rank];
+    const int tid = threadIdx.x, warp = tid >> 5;
     TOut* out = reinterpret_cast<TOut*>(a.out);
 
     int64_t slot = a.state_idx[seq];
@@ -715,14 +743,8 @@ __global__ void __launch_bounds__(128, 1) chunk_state_tc_kernel(const StateArgs 
         tc::tmem_relinquish();
     }
     if (tid == 0) {
-        tc::mbar_init(&bars->w, 1);
-        tc::mbar_init(&bars->kt, 1);
-        tc::mbar_init(&bars->ug, 1);
-        tc::mbar_init(&bars->qb, 1);
-        tc::mbar_init(&bars->p, 1);
-        tc::mbar_init(&bars->mma_a, 1);
-        tc::mbar_init(&bars->mma_c, 1);
-        tc::mbar_init(&bars->drain, 1);
+        uint64_t* b = reinterpret_cast<uint64_t*>(bars);
+        for (int i = 0; i < (int)(sizeof(TcBars) / 8); ++i) tc::mbar_init(b + i, 1);
         *s_abort = 0;
         tc::fence_mbar_init();
     }
@@ -735,23 +757,30 @@ __global__ void __launch_bounds__(128, 1) chunk_state_tc_kernel(const StateArgs 
     auto rec_of = [&](int64_t ch) -> const unsigned char* {
         return reinterpret_cast<const unsigned char*>(a.ws + ((size_t)ch * H + h) * a.ws_stride);
     };
-    // issue the copies of one buffer group for chunk ch (thread 0 only)
-    // copies in flight per buffer (thread 0's bookkeeping, for the drain after a failed wait)
-    uint32_t pend_mask = 0, pend_par = 0;
-    auto load = [&](uint64_t* bar, uint32_t off, uint32_t bytes, int64_t ch) {
-        const uint32_t bit = 1u << (uint32_t)(bar - &bars->w);
+    // copies in flight per load barrier (thread 0's bookkeeping, for the drain after a failed wait)
+    uint64_t* const bar0 = &bars->w[0];
+    uint32_t pend_mask = 0, pend_par = 0, uses[7] = {0, 0, 0, 0, 0, 0, 0};
+    auto load = [&](uint64_t* bar, uint32_t dst_off, uint32_t src_off, uint32_t bytes, int64_t ch) {
+        const uint32_t bi = (uint32_t)(bar - bar0), bit = 1u << bi;
         pend_mask |= bit;
-        pend_par = (pend_par & ~bit) | (((uint32_t)(ch - c_begin) & 1u) ? bit : 0u);
+        pend_par = (pend_par & ~bit) | ((uses[bi] & 1u) ? bit : 0u);
+        ++uses[bi];
         tc::mbar_arrive_expect_tx(bar, bytes);
-        tc::bulk_g2s(sm + off, rec_of(ch) + off, bytes, bar);
+        tc::bulk_g2s(sm + dst_off, rec_of(ch) + src_off, bytes, bar);
     };
-    auto landed = [&](uint64_t* bar) { pend_mask &= ~(1u << (uint32_t)(bar - &bars->w)); };
+    auto landed = [&](uint64_t* bar) { pend_mask &= ~(1u << (uint32_t)(bar - bar0)); };
+    auto w_off = [](uint32_t b) { return b ? kSmW1 : TcRec::W; };
+    auto ug_off = [](uint32_t b) { return b ? kSmUG1 : TcRec::U; };
     if (tid == 0) {
-        load(&bars->w, TcRec::W, 32768, c_begin);
-        load(&bars->ug, TcRec::U, 32768 + 512, c_begin);
-        load(&bars->qb, TcRec::QB, 32768, c_begin);
-        load(&bars->p, TcRec::P, 16384, c_begin);
-        load(&bars->kt, TcRec::KT, 32768, c_begin);
+        load(&bars->w[0], TcRec::W, TcRec::W, 32768, c_begin);
+        load(&bars->ug[0], TcRec::U, TcRec::U, kUGBytes, c_begin);
+        load(&bars->p, TcRec::P, TcRec::P, 16384, c_begin);
+        load(&bars->kt, TcRec::KT, TcRec::KT, 32768, c_begin);
+        load(&bars->qb, TcRec::QB, TcRec::QB, 32768, c_begin);
+        if (c_begin + 1 < c_end) {
+            load(&bars->w[1], kSmW1, TcRec::W, 32768, c_begin + 1);
+            load(&bars->ug[1], kSmUG1, TcRec::U, kUGBytes, c_begin + 1);
+        }
     }
 
     // entry state: row v of S^T = pool[slot][h][v][:]
@@ -767,45 +796,42 @@ __global__ void __launch_bounds__(128, 1) chunk_state_tc_kernel(const StateArgs 
         float t[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) t[j] = tc::round_tf32(S[c + j]);
-        tc::tmem_st16(tmem + lane + kT_SOP + c, t);
+        tc::tmem_st16_nowait(tmem + lane + kT_SOP + c, t);
     }
+    tc::tmem_wait_st();
     tc::tc_fence_before();
     __syncthreads();
 
-    const uint32_t sW = tc::smem_u32(sm + TcRec::W), sQB = tc::smem_u32(sm + TcRec::QB);
+    const uint32_t sQB = tc::smem_u32(sm + TcRec::QB);
     const uint32_t sP = tc::smem_u32(sm + TcRec::P), sKT = tc::smem_u32(sm + TcRec::KT);
-    const float* sU = reinterpret_cast<const float*>(sm + TcRec::U);
-    const float* sG = reinterpret_cast<const float*>(sm + TcRec::GL);
     constexpr uint32_t kId64 = tc::idesc_tf32(128, 64), kId128 = tc::idesc_tf32(128, 128);
     bool ok = true;
 
     for (int64_t ch = c_begin; ch < c_end; ++ch) {
-        const uint32_t ph = (uint32_t)((ch - c_begin) & 1);
-        const bool has_next = ch + 1 < c_end;
+        const uint32_t i = (uint32_t)(ch - c_begin);
+        const uint32_t ph = i & 1u, b = i & 1u, phb = (i >> 1) & 1u;
         const int64_t t0 = a.chunk_start[ch];
         const int L = a.chunk_len[ch];
+        const float* sU = reinterpret_cast<const float*>(sm + ug_off(b));
+        const float* sG = sU + 32768 / 4;
 
-        // (a), (b)
+        // (a)
         if (tid == 0) {
             tc::tc_fence_after();
-            ok = tc::mbar_wait(&bars->w, ph, kWaitPolls) && ok;
-            if (ok) landed(&bars->w);
+            ok = tc::mbar_wait(&bars->w[b], phb, kWaitPolls) && ok;
+            if (ok) landed(&bars->w[b]);
+            const uint32_t sW = tc::smem_u32(sm + w_off(b));
 #pragma unroll
             for (int s = 0; s < D / 8; ++s)
                 tc::mma_tf32_ts(tmem + kT_DD, tmem + kT_SOP + 8 * s, tc::smem_desc(sW + 256 * s, 128, 4096), kId64, s > 0);
             tc::mma_commit(&bars->mma_a);
-            ok = tc::mbar_wait(&bars->qb, ph, kWaitPolls) && ok;
-            if (ok) landed(&bars->qb);
-#pragma unroll
-            for (int s = 0; s < D / 8; ++s)
-                tc::mma_tf32_ts(tmem + kT_OUT, tmem + kT_SOP + 8 * s, tc::smem_desc(sQB + 256 * s, 128, 4096), kId64, s > 0);
             if (!ok) *s_abort = 1;
         }
         // Delta^T = U^T - S^T W^T, rounded copy to TMEM; decay S^T by e^{G_L}
         {
-            const bool okw = tc::mbar_wait(&bars->ug, ph, kWaitPolls) && tc::mbar_wait(&bars->mma_a, ph, kWaitPolls);
+            const bool okw = tc::mbar_wait(&bars->ug[b], phb, kWaitPolls) && tc::mbar_wait(&bars->mma_a, ph, kWaitPolls);
             if (!okw) *s_abort = 1;
-            if (okw && tid == 0) landed(&bars->ug);
+            if (okw && tid == 0) landed(&bars->ug[b]);
             tc::tc_fence_after();
 #pragma unroll
             for (int r0 = 0; r0 < C; r0 += 16) {
@@ -813,31 +839,37 @@ __global__ void __launch_bounds__(128, 1) chunk_state_tc_kernel(const StateArgs 
                 tc::tmem_ld16(tmem + lane + kT_DD + r0, d);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) d[j] = tc::round_tf32(sU[(r0 + j) * D + tid] - d[j]);
-                tc::tmem_st16(tmem + lane + kT_DOP + r0, d);
+                tc::tmem_st16_nowait(tmem + lane + kT_DOP + r0, d);
             }
+            tc::tmem_wait_st();
 #pragma unroll
             for (int c = 0; c < D; ++c) S[c] *= sG[c];
         }
         tc::tc_fence_before();
         __syncthreads();
         if (*s_abort) break;
-        // refill W and U/gL for the next chunk; (b2), (c)
+        // refill W and U/gL of buffer b with chunk i + 2; (b2), (c), (b)
         if (tid == 0) {
             tc::tc_fence_after();
-            if (has_next) {
-                load(&bars->w, TcRec::W, 32768, ch + 1);
-                load(&bars->ug, TcRec::U, 32768 + 512, ch + 1);
+            if (ch + 2 < c_end) {
+                load(&bars->w[b], w_off(b), TcRec::W, 32768, ch + 2);
+                load(&bars->ug[b], ug_off(b), TcRec::U, kUGBytes, ch + 2);
             }
             ok = tc::mbar_wait(&bars->p, ph, kWaitPolls) && ok;
             if (ok) landed(&bars->p);
 #pragma unroll
             for (int s = 0; s < C / 8; ++s)
-                tc::mma_tf32_ts(tmem + kT_OUT, tmem + kT_DOP + 8 * s, tc::smem_desc(sP + 256 * s, 128, 2048), kId64, 1);
+                tc::mma_tf32_ts(tmem + kT_OUT, tmem + kT_DOP + 8 * s, tc::smem_desc(sP + 256 * s, 128, 2048), kId64, s > 0);
             ok = tc::mbar_wait(&bars->kt, ph, kWaitPolls) && ok;
             if (ok) landed(&bars->kt);
 #pragma unroll
             for (int s = 0; s < C / 8; ++s)
                 tc::mma_tf32_ts(tmem + kT_SC, tmem + kT_DOP + 8 * s, tc::smem_desc(sKT + 256 * s, 128, 2048), kId128, s > 0);
+            ok = tc::mbar_wait(&bars->qb, ph, kWaitPolls) && ok;
+            if (ok) landed(&bars->qb);
+#pragma unroll
+            for (int s = 0; s < D / 8; ++s)
+                tc::mma_tf32_ts(tmem + kT_OUT, tmem + kT_SOP + 8 * s, tc::smem_desc(sQB + 256 * s, 128, 4096), kId64, 1);
             tc::mma_commit(&bars->mma_c);
             if (!ok) *s_abort = 1;
         }
@@ -854,7 +886,7 @@ __global__ void __launch_bounds__(128, 1) chunk_state_tc_kernel(const StateArgs 
                     S[c + j] += d[j];
                     d[j] = tc::round_tf32(S[c + j]);
                 }
-                tc::tmem_st16(tmem + lane + kT_SOP + c, d);
+                tc::tmem_st16_nowait(tmem + lane + kT_SOP + c, d);
             }
 #pragma unroll
             for (int r0 = 0; r0 < C; r0 += 16) {
@@ -864,15 +896,16 @@ __global__ void __launch_bounds__(128, 1) chunk_state_tc_kernel(const StateArgs 
                 for (int j = 0; j < 16; ++j)
                     if (r0 + j < L) out[((size_t)(t0 + r0 + j) * H + h) * D + tid] = from_f32<TOut>(o[j]);
             }
+            tc::tmem_wait_st();
         }
         tc::tc_fence_before();
         __syncthreads();
         if (*s_abort) break;
-        if (tid == 0 && has_next) {
+        if (tid == 0 && ch + 1 < c_end) {
             tc::tc_fence_after();
-            load(&bars->qb, TcRec::QB, 32768, ch + 1);
-            load(&bars->p, TcRec::P, 16384, ch + 1);
-            load(&bars->kt, TcRec::KT, 32768, ch + 1);
+            load(&bars->p, TcRec::P, TcRec::P, 16384, ch + 1);
+            load(&bars->kt, TcRec::KT, TcRec::KT, 32768, ch + 1);
+            load(&bars->qb, TcRec::QB, TcRec::QB, 32768, ch + 1);
         }
     }
 
@@ -883,8 +916,8 @@ __global__ void __launch_bounds__(128, 1) chunk_state_tc_kernel(const StateArgs 
             record_error(kDevErrTimeout);
             tc::mma_commit(&bars->drain);
             tc::mbar_wait(&bars->drain, 0, kWaitPolls);
-            for (uint32_t b = 0; b < 5; ++b)
-                if (pend_mask & (1u << b)) tc::mbar_wait(&bars->w + b, (pend_par >> b) & 1u, kWaitPolls);
+            for (uint32_t bi = 0; bi < 7; ++bi)
+                if (pend_mask & (1u << bi)) tc::mbar_wait(bar0 + bi, (pend_par >> bi) & 1u, kWaitPolls);
         }
     } else {
         float* Sd = a.pool + ((size_t)slot * H + h) * (size_t)D * D + (size_t)tid * D;
@@ -901,11 +934,13 @@ __global__ void __launch_bounds__(128, 1) chunk_state_tc_kernel(const StateArgs 
 
 // ---- intra-chunk kernel for bf16 inputs at C = 64, D = 128 ----------------------------------------
 // One CTA of 512 threads per (chunk, head), writing the tensor-core record (TcRec).
-//   1. loads; alpha = e^{g}; L2 norms
-//   2. diagonal 16 x 16 sub-blocks of A and P (running products of alphas, CUDA cores)
+//   1. loads; alpha = e^{g} (MUFU form of the gate); L2 norms
+//   2. diagonal 16 x 16 sub-blocks of A and P: running products of alphas (CUDA cores)
 //   3. per (column, sub-block) products: k o Rin, q o Rin, k o Rout and the block products
-//   4. off-diagonal sub-blocks of A and P (CUDA cores)
-//   5. Qbar, Ktil^T, P images and e^{G_L} into the record
+//   4. off-diagonal sub-blocks of A and P on tcgen05, all three row blocks in one MMA: TMEM lane
+//      m holds key j decayed to the start of row block I (m <-> (I, j), 96 rows), the B image holds
+//      the rows of k o Rin and q o Rin of blocks 1..3 (N = 96); only the I(m) = I(n) part is kept
+//   5. Qbar, Ktil^T, P images and e^{G_L} into the record (overlapping the MMA)
 //   6. T = (I + A)^{-1} by blocks: 16 x 16 diagonal blocks by forward substitution, then
 //      T_IJ = -T_II sum_{J<=K<I} A_IK T_KJ
 //   7. tcgen05: U^T = (beta V)^T T^T and W^T = (beta Kbar)^T T^T (M = 128, N = 64, K = 64)
@@ -917,21 +952,28 @@ constexpr int LDA = 68;   // padded row stride of the [C][C] tiles
 constexpr uint32_t OFF_K = 0;                                   // k_hat -> k o Rin     [C][LD]
 constexpr uint32_t OFF_Q = OFF_K + C * LD * 4;                  // q_hat -> q o Rin     [C][LD]
 constexpr uint32_t OFF_AL = OFF_Q + C * LD * 4;                 // alpha -> k o Rout    [C][LD]
-constexpr uint32_t OFF_V = OFF_AL + C * LD * 4;                 // v bf16               [C][D]
-constexpr uint32_t OFF_A = OFF_V + C * D * 2;                   // A                    [C][LDA]
+constexpr uint32_t OFF_A = OFF_AL + C * LD * 4;                 // A                    [C][LDA]
 constexpr uint32_t OFF_P = OFF_A + C * LDA * 4;                 // P                    [C][LDA]
-constexpr uint32_t OFF_T = OFF_P + C * LDA * 4;                 // T = (I + A)^{-1}     [C][LDA]
-constexpr uint32_t OFF_IT = OFF_T + C * LDA * 4;                // T image (rows r, K = j)
-constexpr uint32_t OFF_BP = OFF_IT + C * C * 4;                 // block products       [NB][D]
+constexpr uint32_t OFF_R1 = OFF_P + C * LDA * 4;                // Gram B image, later T and its image
+constexpr uint32_t R1_BYTES = 96 * D * 4;
+constexpr uint32_t OFF_T = OFF_R1;                              // T = (I + A)^{-1}     [C][LDA]
+constexpr uint32_t OFF_IT = OFF_R1 + C * LDA * 4;               // T image (rows r, K = j)
+constexpr uint32_t OFF_BP = OFF_R1 + R1_BYTES;                  // block products       [NB][D]
 constexpr uint32_t OFF_X = OFF_BP + NB * D * 4;                 // 3 scratch 16 x 16 blocks
 constexpr uint32_t OFF_BETA = OFF_X + 3 * 256 * 4;              // beta                 [C]
-constexpr uint32_t OFF_RN = OFF_BETA + C * 4;                   // 1/|k|, scale/|q|     [2][C]
-constexpr uint32_t OFF_BAR = OFF_RN + 2 * C * 4;                // mbarrier
-constexpr uint32_t OFF_TM = OFF_BAR + 8;                        // TMEM base
-constexpr uint32_t BYTES = OFF_TM + 8;
+constexpr uint32_t OFF_V = OFF_BETA + C * 4;                    // v bf16               [C][D]
+constexpr uint32_t OFF_BAR = OFF_V + C * D * 2;                 // 2 mbarriers
+constexpr uint32_t OFF_TM = OFF_BAR + 16;                       // TMEM base
+constexpr uint32_t BYTES = OFF_TM + 16;
 constexpr uint32_t OFF_IV = OFF_Q;    // (beta V)^T image, rows v, K = j (over q o Rin, free by then)
 constexpr uint32_t OFF_IK = OFF_AL;   // (beta Kbar)^T image, rows c, K = j (over k o Rout)
-static_assert(C * D * 4 <= C * LD * 4, "image fits");
+static_assert(OFF_IT + C * C * 4 <= OFF_R1 + R1_BYTES, "T and its image fit in R1");
+// TMEM columns (512 allocated)
+constexpr uint32_t T_KD = 0;      // decayed keys, A operand of the Gram MMA (128 cols, lanes 0..95)
+constexpr uint32_t T_G = 128;     // Gram result (96 cols)
+constexpr uint32_t T_U = 256;     // U^T (64)
+constexpr uint32_t T_W = 320;     // W^T (64)
+
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 __device__ __forceinline__ float4 mul4(float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); }
@@ -944,6 +986,36 @@ __device__ __forceinline__ float dot4(float4 a, float4 b, float acc)
     acc = fmaf(a.x, b.x, acc); acc = fmaf(a.y, b.y, acc); acc = fmaf(a.z, b.z, acc);
     return fmaf(a.w, b.w, acc);
 }
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2_approx(float x)
+{
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// alpha = e^{g} from the identities e^{-r softplus(x)} = 2^{-r log2(1 + 2^{x log2 e})} and
+// e^{lb sigmoid(r x)} = 2^{lb log2 e / (1 + 2^{-r x log2 e})}, on the special-function unit.
+__device__ __forceinline__ float alpha_mufu(float x, float rate, const GateParams& gp)
+{
+    constexpr float kLog2e = 1.4426950408889634f;
+    if (gp.use_lower_bound) {
+        const float sig = __fdividef(1.0f, 1.0f + ex2_approx(-rate * x * kLog2e));
+        return ex2_approx(gp.lower_bound * kLog2e * sig);
+    }
+    const float sp2 = x > gp.softplus_threshold ? x * kLog2e : lg2_approx(1.0f + ex2_approx(x * kLog2e));
+    return ex2_approx(-rate * sp2);
+}
+// Gram row m (0..95) -> row block I and key row j
+__device__ __forceinline__ void gram_row(int m, int& I, int& j)
+{
+    I = m < 16 ? 1 : (m < 48 ? 2 : 3);
+    j = m - (I == 1 ? 0 : (I == 2 ? 16 : 48));
+}
 }  // namespace itc
 
 __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const IntraArgs a)
@@ -954,16 +1026,16 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
     float* sK = reinterpret_cast<float*>(sm + OFF_K);
     float* sQ = reinterpret_cast<float*>(sm + OFF_Q);
     float* sAl = reinterpret_cast<float*>(sm + OFF_AL);
-    __nv_bfloat16* sV = reinterpret_cast<__nv_bfloat16*>(sm + OFF_V);
     float* sA = reinterpret_cast<float*>(sm + OFF_A);
     float* sP = reinterpret_cast<float*>(sm + OFF_P);
+    float* sB = reinterpret_cast<float*>(sm + OFF_R1);
     float* sT = reinterpret_cast<float*>(sm + OFF_T);
     float* sIT = reinterpret_cast<float*>(sm + OFF_IT);
     float* sBp = reinterpret_cast<float*>(sm + OFF_BP);
     float* sX = reinterpret_cast<float*>(sm + OFF_X);
     float* sBeta = reinterpret_cast<float*>(sm + OFF_BETA);
-    float* sRn = reinterpret_cast<float*>(sm + OFF_RN);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    uint64_t* bar_g = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    uint64_t* bar_uw = bar_g + 1;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + OFF_TM);
 
     const int64_t ch = blockIdx.x;
@@ -984,52 +1056,71 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
     const __nv_bfloat16* vp = reinterpret_cast<const __nv_bfloat16*>(a.v);
 
     if (warp == 0) {
-        tc::tmem_alloc(s_tmem, 128);
+        tc::tmem_alloc(s_tmem, 512);
         tc::tmem_relinquish();
     }
     if (tid == 0) {
-        tc::mbar_init(bar, 1);
+        tc::mbar_init(bar_g, 1);
+        tc::mbar_init(bar_uw, 1);
         tc::fence_mbar_init();
     }
 
-    // 1. loads (rows past the chunk end: k = q = v = 0, alpha = 1, beta = 0)
-    for (int e = tid; e < C * D / 8; e += THREADS) {
-        const int r = e >> 4, c8 = (e & 15) * 8;
-        uint4 kv = make_uint4(0, 0, 0, 0), qv = kv, vv = kv;
-        if (r < L) {
-            const size_t idx = ((size_t)(t0 + r) * H + h) * D + c8;
-            kv = *reinterpret_cast<const uint4*>(kp + idx);
-            qv = *reinterpret_cast<const uint4*>(qp + idx);
-            vv = *reinterpret_cast<const uint4*>(vp + idx);
-        }
-        const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&kv);
-        const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(&qv);
-        float kf[8], qf[8];
+    // 1. loads, all issued before any is used (rows past the chunk end: k = q = v = 0, alpha = 1,
+    //    beta = 0); thread e handles 8 elements of k, q, v and 4 + 4 of g in rows e >> 4 and (e >> 4) + 32
+    __nv_bfloat16* sV = reinterpret_cast<__nv_bfloat16*>(sm + OFF_V);
+    {
+        uint4 kv[2], qv[2], vv[2];
+        float4 gv[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) { kf[i] = __bfloat162float(kb[i]); qf[i] = __bfloat162float(qb[i]); }
-        st4(sK + r * LD + c8, make_float4(kf[0], kf[1], kf[2], kf[3]));
-        st4(sK + r * LD + c8 + 4, make_float4(kf[4], kf[5], kf[6], kf[7]));
-        st4(sQ + r * LD + c8, make_float4(qf[0], qf[1], qf[2], qf[3]));
-        st4(sQ + r * LD + c8 + 4, make_float4(qf[4], qf[5], qf[6], qf[7]));
-        *reinterpret_cast<uint4*>(sV + r * D + c8) = vv;
-    }
-    for (int e = tid; e < C * D / 4; e += THREADS) {
-        const int r = e >> 5, c4 = (e & 31) * 4;
-        float4 al = make_float4(1.f, 1.f, 1.f, 1.f);
-        if (r < L) {
-            const size_t idx = ((size_t)(t0 + r) * H + h) * D + c4;
-            const float4 g = *reinterpret_cast<const float4*>(a.g_raw + idx);
-            float4 db = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (a.dt_bias) db = *reinterpret_cast<const float4*>(a.dt_bias + (size_t)h * D + c4);
-            al.x = expf(gate_log_decay(g.x + db.x, rate, a.gp));
-            al.y = expf(gate_log_decay(g.y + db.y, rate, a.gp));
-            al.z = expf(gate_log_decay(g.z + db.z, rate, a.gp));
-            al.w = expf(gate_log_decay(g.w + db.w, rate, a.gp));
+        for (int i = 0; i < 2; ++i) {
+            const int e = tid + i * THREADS, r = e >> 4, c8 = (e & 15) * 8;
+            kv[i] = qv[i] = vv[i] = make_uint4(0, 0, 0, 0);
+            if (r < L) {
+                const size_t idx = ((size_t)(t0 + r) * H + h) * D + c8;
+                kv[i] = *reinterpret_cast<const uint4*>(kp + idx);
+                qv[i] = *reinterpret_cast<const uint4*>(qp + idx);
+                vv[i] = *reinterpret_cast<const uint4*>(vp + idx);
+            }
         }
-        st4(sAl + r * LD + c4, al);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int e = tid + i * THREADS, r = e >> 5, c4 = (e & 31) * 4;
+            gv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r < L) gv[i] = *reinterpret_cast<const float4*>(a.g_raw + ((size_t)(t0 + r) * H + h) * D + c4);
+        }
+        float bt = 0.f;
+        if (tid < L) bt = a.b_raw[(size_t)(t0 + tid) * H + h];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int e = tid + i * THREADS, r = e >> 4, c8 = (e & 15) * 8;
+            const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&kv[i]);
+            const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(&qv[i]);
+            float kf[8], qf[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) { kf[t] = __bfloat162float(kb[t]); qf[t] = __bfloat162float(qb[t]); }
+            st4(sK + r * LD + c8, make_float4(kf[0], kf[1], kf[2], kf[3]));
+            st4(sK + r * LD + c8 + 4, make_float4(kf[4], kf[5], kf[6], kf[7]));
+            st4(sQ + r * LD + c8, make_float4(qf[0], qf[1], qf[2], qf[3]));
+            st4(sQ + r * LD + c8 + 4, make_float4(qf[4], qf[5], qf[6], qf[7]));
+            *reinterpret_cast<uint4*>(sV + r * D + c8) = vv[i];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int e = tid + i * THREADS, r = e >> 5, c4 = (e & 31) * 4;
+            float4 al = make_float4(1.f, 1.f, 1.f, 1.f);
+            if (r < L) {
+                float4 db = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (a.dt_bias) db = *reinterpret_cast<const float4*>(a.dt_bias + (size_t)h * D + c4);
+                al.x = alpha_mufu(gv[i].x + db.x, rate, a.gp);
+                al.y = alpha_mufu(gv[i].y + db.y, rate, a.gp);
+                al.z = alpha_mufu(gv[i].z + db.z, rate, a.gp);
+                al.w = alpha_mufu(gv[i].w + db.w, rate, a.gp);
+            }
+            st4(sAl + r * LD + c4, al);
+        }
+        if (tid < C) sBeta[tid] = tid < L ? sigmoid_f32(bt) : 0.f;
     }
-    if (tid < C) sBeta[tid] = tid < L ? sigmoid_f32(a.b_raw[(size_t)(t0 + tid) * H + h]) : 0.f;
-    for (int e = tid; e < C * LDA; e += THREADS) { sA[e] = 0.f; sP[e] = 0.f; sT[e] = 0.f; }
+    for (int e = tid; e < C * LDA; e += THREADS) { sA[e] = 0.f; sP[e] = 0.f; }
     __syncthreads();
     for (int r = warp; r < C; r += THREADS / 32) {
         const float4 k4 = ld4(sK + r * LD + lane * 4), q4 = ld4(sQ + r * LD + lane * 4);
@@ -1045,14 +1136,17 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
     }
     __syncthreads();
 
-    // 2. diagonal sub-blocks: thread (row j, column group cg), columns 4 cg + 32 m
+    // 2. diagonal sub-blocks: thread (row j, column group cg), columns 4 cg + 32 m.  A warp holds
+    //    rows j = 4w .. 4w + 3, so rows r below the warp's first j are skipped uniformly.
     {
         const int j = tid >> 3, cg = tid & 7, blk0 = j & ~15;
+        const int rstart = (j & 15) & ~3;
         float4 kd[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) kd[m] = ld4(sK + j * LD + 4 * cg + 32 * m);
-#pragma unroll 1
+#pragma unroll
         for (int rr = 0; rr < 16; ++rr) {
+            if (rr < rstart) continue;
             const int r = blk0 + rr;
             float pa = 0.f, pp = 0.f;
 #pragma unroll
@@ -1103,26 +1197,51 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
     }
     __syncthreads();
 
-    // 4. off-diagonal sub-blocks (I, J), J < I: decay = Rin_I(r) * M_IJ * Rout_J(j)
-    for (int e = tid; e < 6 * 256; e += THREADS) {
-        const int bpi = e >> 8;
-        const int I = bpi == 0 ? 1 : (bpi < 3 ? 2 : 3);
-        const int J = bpi == 0 ? 0 : (bpi < 3 ? bpi - 1 : bpi - 3);
-        const int r = 16 * I + ((e >> 4) & 15), j = 16 * J + (e & 15);
-        float pa = 0.f, pp = 0.f;
-#pragma unroll 4
-        for (int c = 0; c < D; c += 4) {
-            float4 ko = ld4(sAl + j * LD + c);
-            for (int bb = J + 1; bb < I; ++bb) ko = mul4(ko, ld4(sBp + bb * D + c));
-            pa = dot4(ld4(sK + r * LD + c), ko, pa);
-            pp = dot4(ld4(sQ + r * LD + c), ko, pp);
-        }
-        sA[r * LDA + j] = sBeta[r] * pa;
-        sP[r * LDA + j] = pp;
-    }
-    __syncthreads();
+    const uint32_t tmem = *s_tmem;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-    // 5. record: Qbar image, Ktil^T image, P image, e^{G_L}
+    // 4a. Gram operands: B image rows n = 32 (I - 1) + {0..15: k o Rin, 16..31: q o Rin} of row block I;
+    //     TMEM lane m <- key j decayed to the start of block I: (k o Rout)[j] * prod_{J < bb < I} bp[bb]
+    for (int f = tid; f < 96 * D / 4; f += THREADS) {
+        const int core = f >> 3, n = (core >> 5) * 8 + (f & 7), c = (core & 31) * 4;
+        const int I = (n >> 5) + 1, w = n & 31;
+        const int r = 16 * I + (w & 15);
+        st4(sB + 4 * f, rnd4(ld4((w < 16 ? sK : sQ) + r * LD + c)));
+    }
+    if ((warp & 3) < 3) {          // lanes 0..95; warp quarter (warp >> 2) writes columns 32 q .. 32 q + 31
+        const int m = (warp & 3) * 32 + lane;
+        int I, j;
+        gram_row(m, I, j);
+        const int J = j >> 4;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int c0 = (warp >> 2) * 32 + 16 * h2;
+            float x[16];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float4 v = ld4(sAl + j * LD + c0 + 4 * q4);
+                for (int bb = J + 1; bb < I; ++bb) v = mul4(v, ld4(sBp + bb * D + c0 + 4 * q4));
+                v = rnd4(v);
+                x[4 * q4] = v.x; x[4 * q4 + 1] = v.y; x[4 * q4 + 2] = v.z; x[4 * q4 + 3] = v.w;
+            }
+            tc::tmem_st16_nowait(tmem + lane_base + T_KD + c0, x);
+        }
+        tc::tmem_wait_st();
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc::tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+        tc::tc_fence_after();
+        const uint32_t bB = tc::smem_u32(sB);
+        constexpr uint32_t idesc = tc::idesc_tf32(128, 96);
+#pragma unroll
+        for (int s = 0; s < D / 8; ++s)
+            tc::mma_tf32_ts(tmem + T_G, tmem + T_KD + 8 * s, tc::smem_desc(bB + 256 * s, 128, D * 32), idesc, s > 0);
+        tc::mma_commit(bar_g);
+    }
+
+    // 5. record: Qbar image, Ktil^T image, e^{G_L} (while the Gram MMA runs)
     unsigned char* rec = reinterpret_cast<unsigned char*>(a.ws + ((size_t)ch * H + h) * a.ws_stride);
     float* wW = reinterpret_cast<float*>(rec + TcRec::W);
     float* wKT = reinterpret_cast<float*>(rec + TcRec::KT);
@@ -1144,19 +1263,47 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
                                      sAl[(r0 + 2) * LD + cc] * ea, sAl[(r0 + 3) * LD + cc] * ea);
         st4(wKT + 4 * f, rnd4(v));
     }
-    for (int f = tid; f < C * C / 4; f += THREADS) {          // P: rows r, K = j
-        const int core = f >> 3, rr = (core >> 4) * 8 + (f & 7), j0 = (core & 15) * 4;
-        st4(wP + 4 * f, rnd4(ld4(sP + rr * LDA + j0)));
-    }
     if (tid < D) {
         float gL = 1.f;
 #pragma unroll
         for (int bb = 0; bb < NB; ++bb) gL *= sBp[bb * D + tid];
         wG[tid] = gL;
     }
+    // 4b. Gram result -> off-diagonal blocks of A and P
+    if (warp < 3) {
+        const bool done = tc::mbar_wait(bar_g, 0, kWaitPolls);
+        tc::tc_fence_after();
+        if (!done && lane == 0) record_error(kDevErrTimeout);
+        const int m = tid;
+        int I, j;
+        gram_row(m, I, j);
+        float g[96];
+        tc::tmem_ld32(tmem + lane_base + T_G, g);
+        tc::tmem_ld32(tmem + lane_base + T_G + 32, g + 32);
+        tc::tmem_ld32(tmem + lane_base + T_G + 64, g + 64);
+#pragma unroll
+        for (int Ib = 1; Ib <= 3; ++Ib) {
+            if (Ib == I) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int r = 16 * I + i;
+                    sA[r * LDA + j] = sBeta[r] * g[32 * (Ib - 1) + i];
+                    sP[r * LDA + j] = g[32 * (Ib - 1) + 16 + i];
+                }
+            }
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
 
-    // 6. T = (I + A)^{-1}
-    if (tid < C) {                                            // diagonal blocks, one column each
+    // P image (rows r, K = j); T diagonal blocks (R1 is free: the Gram MMA has completed)
+    for (int f = tid; f < C * C / 4; f += THREADS) {
+        const int core = f >> 3, rr = (core >> 4) * 8 + (f & 7), j0 = (core & 15) * 4;
+        st4(wP + 4 * f, rnd4(ld4(sP + rr * LDA + j0)));
+    }
+    for (int e = tid; e < C * LDA; e += THREADS) sT[e] = 0.f;
+    __syncthreads();
+    if (tid < C) {
         const int I = tid >> 4, jj = tid & 15, j = tid;
         float col[16];
 #pragma unroll
@@ -1172,6 +1319,7 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
         for (int i = 0; i < 16; ++i) sT[(16 * I + i) * LDA + j] = col[i];
     }
     __syncthreads();
+    // 6. off-diagonal blocks of T
     for (int d = 1; d < NB; ++d) {
         const int nb = NB - d;
         for (int e = tid; e < nb * 256; e += THREADS) {      // X_IJ = sum_{J<=K<I} A_IK T_KJ
@@ -1206,8 +1354,9 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
         for (int bb = 0; bb < (j0 >> 4); ++bb) eb *= sBp[bb * D + row];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            pv[i] = sBeta[j0 + i] * __bfloat162float(sV[(j0 + i) * D + row]);
-            pk[i] = sBeta[j0 + i] * sK[(j0 + i) * LD + row] * eb;
+            const int j = j0 + i;
+            pv[i] = sBeta[j] * __bfloat162float(sV[j * D + row]);
+            pk[i] = sBeta[j] * sK[j * LD + row] * eb;
         }
         st4(sIV + 4 * f, rnd4(vv));
         st4(sIK + 4 * f, rnd4(kb));
@@ -1215,29 +1364,28 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc::tc_fence_before();
     __syncthreads();
-    tc::tc_fence_after();
-    const uint32_t tmem = *s_tmem;
 
-    // 8. U^T = (beta V)^T T^T (TMEM columns 0..63), W^T = (beta Kbar)^T T^T (columns 64..127)
+    // 8. U^T = (beta V)^T T^T, W^T = (beta Kbar)^T T^T
     if (tid == 0) {
+        tc::tc_fence_after();
         constexpr uint32_t idesc = tc::idesc_tf32(128, 64);
         const uint32_t aV = tc::smem_u32(sIV), aK = tc::smem_u32(sIK), bT = tc::smem_u32(sIT);
 #pragma unroll
         for (int s = 0; s < C / 8; ++s)
-            tc::mma_tf32_ss(tmem, tc::smem_desc(aV + 256 * s, 128, 2048), tc::smem_desc(bT + 256 * s, 128, 2048), idesc, s > 0);
+            tc::mma_tf32_ss(tmem + T_U, tc::smem_desc(aV + 256 * s, 128, 2048), tc::smem_desc(bT + 256 * s, 128, 2048), idesc, s > 0);
 #pragma unroll
         for (int s = 0; s < C / 8; ++s)
-            tc::mma_tf32_ss(tmem + 64, tc::smem_desc(aK + 256 * s, 128, 2048), tc::smem_desc(bT + 256 * s, 128, 2048), idesc, s > 0);
-        tc::mma_commit(bar);
+            tc::mma_tf32_ss(tmem + T_W, tc::smem_desc(aK + 256 * s, 128, 2048), tc::smem_desc(bT + 256 * s, 128, 2048), idesc, s > 0);
+        tc::mma_commit(bar_uw);
     }
     if (warp < 8) {
-        const bool done = tc::mbar_wait(bar, 0, kWaitPolls);
+        const bool done = tc::mbar_wait(bar_uw, 0, kWaitPolls);
         tc::tc_fence_after();
         if (!done) {
             if (lane == 0) record_error(kDevErrTimeout);
         } else {
             const int row = (warp & 3) * 32 + lane;
-            const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (warp < 4 ? 0u : 64u);
+            const uint32_t taddr = tmem + lane_base + (warp < 4 ? T_U : T_W);
 #pragma unroll
             for (int r0 = 0; r0 < C; r0 += 16) {
                 float x[16];
@@ -1256,7 +1404,7 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
     __syncthreads();
     if (warp == 0) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem, 128);
+        tc::tmem_dealloc(tmem, 512);
     }
 }
 
@@ -1275,11 +1423,13 @@ cudaError_t run_prefill(const kda_params& p, const GateParams& gp, const void* q
     int32_t* chunk_start = tab + w.max_chunks;
     int32_t* chunk_len = tab + 2 * w.max_chunks;
     int32_t* seq_off = tab + 3 * w.max_chunks;
+    int32_t* seq_order = seq_off + N + 1;
     float* ws = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + w.table_bytes);
 
     cudaError_t e;
     if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
-    chunk_table_kernel<<<1, 1024, 0, stream>>>(cu, N, T, C, w.max_chunks, chunk_seq, chunk_start, chunk_len, seq_off);
+    chunk_table_kernel<<<1, 1024, 0, stream>>>(cu, N, T, C, w.max_chunks, chunk_seq, chunk_start, chunk_len, seq_off,
+                                               seq_order);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return e;
@@ -1310,6 +1460,7 @@ cudaError_t run_prefill(const kda_params& p, const GateParams& gp, const void* q
     if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return e;
 
     StateArgs sa;
+    sa.seq_order = seq_order;
     sa.chunk_start = chunk_start; sa.chunk_len = chunk_len; sa.seq_off = seq_off; sa.cu = cu;
     sa.state_idx = state_idx; sa.pool = pool; sa.num_slots = num_slots; sa.max_chunks = w.max_chunks;
     sa.T = T; sa.N = N; sa.H = H; sa.ws = ws; sa.ws_stride = w.per_chunk_head; sa.out = out;
@@ -1317,8 +1468,7 @@ cudaError_t run_prefill(const kda_params& p, const GateParams& gp, const void* q
         auto state = chunk_state_tc_kernel<TOut>;
         e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmemBytes);
         if (e != cudaSuccess) return e;
-        dim3 gs((unsigned)N, (unsigned)H);
-        state<<<gs, 128, kTcSmemBytes, stream>>>(sa);
+        state<<<(unsigned)((int64_t)N * H), 128, kTcSmemBytes, stream>>>(sa);
     } else {
         constexpr int NV = D < 32 ? D : 32;
         using SS = StateShape<C, D, NV>;
