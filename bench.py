@@ -33,6 +33,30 @@ METRIC = "prefill tokens/s and decode tokens/s (state GB/s, % HBM/tensor rooflin
 UNIT = "tokens/s"
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, one ncu capture of a bench
+# step, caches flushed before each kernel), valid only for the kernel source they were taken on.
+MEASURED_TRAFFIC = {
+    "kda_prefill.cu": {"sha256_16": "0a685b26ba862479",
+                       "kda_chunk_table": 0.0, "kda_chunk_intra": 1870.8e6, "kda_chunk_state": 1392.4e6},
+    "kda_recurrent.cu": {"sha256_16": "3c74368449a48cdc",
+                         "kda_recurrent_decode": 1022.6e6, "kda_recurrent_verify": 614.8e6},
+}
+
+
+def measured_traffic(kernel):
+    """Bytes per launch from the stored capture, or None if the kernel's source changed since."""
+    import hashlib
+    for src, rec in MEASURED_TRAFFIC.items():
+        if kernel in rec:
+            path = os.path.join(ROOT, "kda_gated_delta_gb300", "csrc", src)
+            try:
+                h = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+            except OSError:
+                return None
+            return rec[kernel] if h == rec["sha256_16"] else None
+    return None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -182,14 +206,33 @@ def oracle_prefill_sample(n_tokens):
     return time.perf_counter() - t0, threads
 
 
-def cpu_baseline(target_s=12.0):
-    """Time the oracle as it stands on a bounded sample (about target_s seconds of CPU work)."""
-    t, thr = oracle_prefill_sample(32)
-    n = int(max(32, min(4096, 32 * target_s / max(t, 1e-3))))
-    t, thr = oracle_prefill_sample(n)
-    return {"value": n / t, "unit": UNIT, "cores": thr, "kind": "oracle",
-            "sample": f"fp64 token recurrence over the first {n} tokens of the varlen workload's first "
-                      f"sequence, all 32 heads (threads over heads), {t:.1f} s"}
+def oracle_workload_once():
+    """Oracle over the whole varlen workload (8 sequences, all 32 heads, threads over heads)."""
+    import oracle
+    from kda_gated_delta_gb300 import workloads
+
+    if "inp" not in _PREFILL_HOST:
+        _PREFILL_HOST["inp"] = workloads.workload_inputs(1)
+    inp = _PREFILL_HOST["inp"]
+    threads = min(len(os.sched_getaffinity(0)), 32)
+    p = oracle.make_params(32, 128)
+    t0 = time.perf_counter()
+    oracle.forward(p, inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["b_raw"], inp["A_log"], inp["dt_bias"],
+                   inp["cu_seqlens"], inp["pool"], inp["state_idx"], nthreads=threads)
+    return time.perf_counter() - t0, threads, int(inp["cu_seqlens"][-1])
+
+
+def cpu_baseline(target_s=10.0):
+    """Time the oracle as it stands on a bounded sample: the whole varlen workload, repeated until
+    about target_s seconds of CPU time have been spent."""
+    total, reps, thr, T = 0.0, 0, 1, 0
+    while total < target_s and reps < 64:
+        t, thr, T = oracle_workload_once()
+        total += t
+        reps += 1
+    return {"value": T * reps / total, "unit": UNIT, "cores": thr, "kind": "oracle",
+            "sample": f"fp64 token recurrence over the whole varlen workload ({T} tokens, 8 sequences, "
+                      f"32 heads, threads over heads) x {reps}, {total:.1f} s"}
 
 
 def run_reference(args):
@@ -318,10 +361,13 @@ def run_ours(args):
     dec_value = world * wd.batch / (dec_ms * 1e-3)
     ver_value = world * wv.batch * wv.t_draft / (ver_ms * 1e-3)
 
-    def roof(bytes_, ms):
+    def roof(bytes_, ms, kernels_):
         ach = bytes_ / (ms * 1e-3) / 1e9
+        tr = [measured_traffic(k) for k in kernels_]
         return {"bound": "hbm", "achieved": round(ach, 1), "peak": bw_peak, "unit": "GB/s",
-                "frac": round(ach / bw_peak, 4), "peak_source": f"hbm_gbs ({peak_src})"}
+                "frac": round(ach / bw_peak, 4), "peak_source": f"hbm_gbs ({peak_src})",
+                "algorithmic_bytes": bytes_,
+                "traffic": None if any(t is None for t in tr) else sum(tr)}
 
     kernels = [{"name": n, "ms": round(m, 5)} for n, m in
                zip(("kda_chunk_table", "kda_chunk_intra", "kda_chunk_state"), phase_ms)]
@@ -332,10 +378,9 @@ def run_ours(args):
         k["share"] = round(k["ms"] / tot, 4)
     dominant = max(kernels, key=lambda k: k["ms"])
 
-    roofline = roof(pre_B, pre_ms)
+    roofline = roof(pre_B, pre_ms, ("kda_chunk_table", "kda_chunk_intra", "kda_chunk_state"))
     roofline.update({"scope": "prefill call (chunk_table + chunk_intra + chunk_state), varlen workload",
-                     "algorithmic_bytes": pre_B, "ms": round(pre_ms, 5), "traffic": None,
-                     "dominant_kernel": dominant["name"]})
+                     "ms": round(pre_ms, 5), "dominant_kernel": dominant["name"]})
 
     # ---- end to end: host buffers, copies inside the timed region -----------------------------
     e2e = None
@@ -386,10 +431,10 @@ def run_ours(args):
         "roofline": roofline,
         "decode": {"value": round(dec_value, 1), "unit": UNIT, "ms": round(dec_ms, 5),
                    "state_gbs": round(wd.batch * H * 2 * D * D * 4 / (dec_ms * 1e-3) / 1e9, 1),
-                   "roofline": roof(dec_B, dec_ms),
+                   "roofline": roof(dec_B, dec_ms, ("kda_recurrent_decode",)),
                    "workload": "decode_bf16: 256 requests x 1 token, H=32, d=128, 512-slot fp32 pool"},
         "verify": {"value": round(ver_value, 1), "unit": UNIT, "ms": round(ver_ms, 5),
-                   "roofline": roof(ver_B, ver_ms),
+                   "roofline": roof(ver_B, ver_ms, ("kda_recurrent_verify",)),
                    "workload": "gdn_verify_bf16: 64 requests x 4 drafts, per-head gate, inter states"},
         "kernels": kernels,
         "clocks": clk,

@@ -1,0 +1,68 @@
+"""The replica path of bench.py on two gloo ranks (CPU): rendezvous on 127.0.0.1, the barrier, and
+the max-over-ranks reduction that turns per-rank step times into the job's time.  The hot path
+has no exchange step, so these helpers are the whole multi-rank logic."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    r, w, local = bench.dist_env()
+    dist = bench.maybe_init_dist(w, "gloo")
+    try:
+        bench.barrier(dist)
+        ms = 1.5 + rank                      # each rank's measured step time
+        job_ms = bench.reduce_max(dist, ms, torch.device("cpu"))
+        tokens = 1000                        # units each replica processes
+        value = w * tokens / (job_ms * 1e-3)
+        q.put((r, w, local, job_ms, value))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_replicas_reduce_to_the_slowest_rank():
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(world))
+    for r, (rank, w, local, job_ms, value) in enumerate(res):
+        assert (rank, w, local) == (r, world, r)
+        assert job_ms == pytest.approx(2.5)          # max over ranks
+        assert value == pytest.approx(2 * 1000 / 2.5e-3)
+
+
+def test_single_process_needs_no_process_group():
+    assert bench.maybe_init_dist(1, "gloo") is None
+    assert bench.reduce_max(None, 3.0, torch.device("cpu")) == 3.0
+    bench.barrier(None)
+
+
+def test_algorithmic_byte_counts():
+    """The per-unit byte counts the roofline uses, against the figures written out by hand."""
+    # decode: per (request, head) state read + write, q/k/v bf16, g_raw fp32, b_raw, out bf16
+    assert bench.decode_bytes(1, 1, 128, 2, 2) == 2 * 128 * 128 * 4 + 3 * 256 + 512 + 4 + 256 + 4 + 512
+    # prefill: 1540 bytes per token and head for bf16 in/out, d = 128, plus the state per sequence
+    assert bench.prefill_bytes(1, 0, 1, 128, 2, 2) == 1540 + 4 + 512
+    assert bench.prefill_bytes(0, 1, 1, 128, 2, 2) == 2 * 128 * 128 * 4 + 4 + 512
+    # verify (per-head gate): one state read, per draft one state write and its token's bytes
+    assert bench.verify_bytes(1, 4, 1, 128, 2, 2) == 65536 + 4 * (65536 + 768 + 4 + 4 + 256) + 8
