@@ -934,7 +934,7 @@ __global__ void __launch_bounds__(128, 1) chunk_state_tc_kernel(const StateArgs 
 
 // ---- intra-chunk kernel for bf16 inputs at C = 64, D = 128 ----------------------------------------
 // One CTA of 512 threads per (chunk, head), writing the tensor-core record (TcRec).
-//   1. loads; alpha = e^{g} (MUFU form of the gate); L2 norms
+//   1. loads; alpha = e^{g} (MUFU form of the gate); L2 norms (fused into the loads)
 //   2. diagonal 16 x 16 sub-blocks of A and P: running products of alphas (CUDA cores)
 //   3. per (column, sub-block) products: k o Rin, q o Rin, k o Rout and the block products
 //   4. off-diagonal sub-blocks of A and P on tcgen05, all three row blocks in one MMA: TMEM lane
@@ -1092,12 +1092,26 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
         if (tid < L) bt = a.b_raw[(size_t)(t0 + tid) * H + h];
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
+            // the 16 consecutive lanes that hold row r reduce its squared norms with shuffles
             const int e = tid + i * THREADS, r = e >> 4, c8 = (e & 15) * 8;
             const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&kv[i]);
             const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(&qv[i]);
-            float kf[8], qf[8];
+            float kf[8], qf[8], kk = 0.f, qq = 0.f;
 #pragma unroll
-            for (int t = 0; t < 8; ++t) { kf[t] = __bfloat162float(kb[t]); qf[t] = __bfloat162float(qb[t]); }
+            for (int t = 0; t < 8; ++t) {
+                kf[t] = __bfloat162float(kb[t]);
+                qf[t] = __bfloat162float(qb[t]);
+                kk = fmaf(kf[t], kf[t], kk);
+                qq = fmaf(qf[t], qf[t], qq);
+            }
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) {
+                kk += __shfl_xor_sync(0xffffffffu, kk, off);
+                qq += __shfl_xor_sync(0xffffffffu, qq, off);
+            }
+            const float rk = 1.0f / sqrtf(kk + a.gp.l2_eps), rq = a.gp.scale / sqrtf(qq + a.gp.l2_eps);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) { kf[t] *= rk; qf[t] *= rq; }
             st4(sK + r * LD + c8, make_float4(kf[0], kf[1], kf[2], kf[3]));
             st4(sK + r * LD + c8 + 4, make_float4(kf[4], kf[5], kf[6], kf[7]));
             st4(sQ + r * LD + c8, make_float4(qf[0], qf[1], qf[2], qf[3]));
@@ -1121,19 +1135,6 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
         if (tid < C) sBeta[tid] = tid < L ? sigmoid_f32(bt) : 0.f;
     }
     for (int e = tid; e < C * LDA; e += THREADS) { sA[e] = 0.f; sP[e] = 0.f; }
-    __syncthreads();
-    for (int r = warp; r < C; r += THREADS / 32) {
-        const float4 k4 = ld4(sK + r * LD + lane * 4), q4 = ld4(sQ + r * LD + lane * 4);
-        float kk = dot4(k4, k4, 0.f), qq = dot4(q4, q4, 0.f);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            kk += __shfl_xor_sync(0xffffffffu, kk, off);
-            qq += __shfl_xor_sync(0xffffffffu, qq, off);
-        }
-        const float rk = 1.0f / sqrtf(kk + a.gp.l2_eps), rq = a.gp.scale / sqrtf(qq + a.gp.l2_eps);
-        st4(sK + r * LD + lane * 4, make_float4(k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk));
-        st4(sQ + r * LD + lane * 4, make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq));
-    }
     __syncthreads();
 
     // 2. diagonal sub-blocks: thread (row j, column group cg), columns 4 cg + 32 m.  A warp holds

@@ -74,11 +74,6 @@ recurrent_kernel(const RecArgs a)
     constexpr int NWARPS = Sh::NWARPS, CPL = Sh::CPL, LPR = Sh::LPR, RPS = Sh::RPS;
     constexpr int STEPS = Sh::STEPS, NV4 = Sh::NV4;
 
-    __shared__ float s_k[D];
-    __shared__ float s_q[D];
-    __shared__ float s_alpha[D];
-    __shared__ float s_red[3][NWARPS];
-
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -106,7 +101,7 @@ recurrent_kernel(const RecArgs a)
     const int li = lane % LPR;
     const size_t tile = ((size_t)slot * H + h) * (size_t)D * D;
 
-    // Issue every state load of this thread first; the gate/norm prologue overlaps their latency.
+    // Issue every state load of this thread first; the token prologue overlaps their latency.
     float4 st[STEPS][NV4];
 #pragma unroll
     for (int s = 0; s < STEPS; ++s) {
@@ -116,26 +111,44 @@ recurrent_kernel(const RecArgs a)
         for (int j = 0; j < NV4; ++j) st[s][j] = __ldcs(src + li + LPR * j);
     }
 
+    // ---- prologue for all T tokens at once: inputs to shared memory, then norms, q.k, beta, alpha
+    extern __shared__ float4 rec_smem4[];
+    float* s_k = reinterpret_cast<float*>(rec_smem4);    // [T][D] k -> k_hat
+    float* s_q = s_k + T * D;                            // [T][D] q -> q_hat * scale
+    float* s_al = s_q + T * D;                           // [T][D] alpha (per-channel gate)
+    float* s_v = s_al + T * D;                           // [T][D] v
+    float* s_sc = s_v + T * D;                           // [T][8]: beta, q.k, alpha (per head), 1/|k|, scale/|q|
     const TIn* qp = reinterpret_cast<const TIn*>(a.q);
     const TIn* kp = reinterpret_cast<const TIn*>(a.k);
     const TIn* vp = reinterpret_cast<const TIn*>(a.v);
     const float rate = expf(a.A_log[h]);
-
-    for (int t = 0; t < T; ++t) {
-        const int64_t tok = b * T + t;
-        const size_t rowbase = ((size_t)tok * H + h) * D;
-
-        // ---- prologue: L2 norms, q.k, gate and beta for this token --------------------------
-        float kc = 0.f, qc = 0.f;
-        if (tid < D) {
-            kc = to_f32(kp[rowbase + tid]);
-            qc = to_f32(qp[rowbase + tid]);
-            if (GATE == KDA_GATE_PER_CHANNEL) {
-                const float x = a.g_raw[rowbase + tid] + (a.dt_bias ? a.dt_bias[(size_t)h * D + tid] : 0.f);
-                s_alpha[tid] = expf(gate_log_decay(x, rate, a.gp));
-            }
+    for (int e = tid; e < T * D; e += Sh::THREADS) {
+        const int t = e / D, c = e - t * D;
+        const size_t idx = ((size_t)(b * T + t) * H + h) * D + c;
+        s_k[e] = to_f32(kp[idx]);
+        s_q[e] = to_f32(qp[idx]);
+        s_v[e] = to_f32(vp[idx]);
+        if (GATE == KDA_GATE_PER_CHANNEL) {
+            const float x = a.g_raw[idx] + (a.dt_bias ? a.dt_bias[(size_t)h * D + c] : 0.f);
+            s_al[e] = expf(gate_log_decay(x, rate, a.gp));
         }
-        float kk = kc * kc, qq = qc * qc, kq = kc * qc;
+    }
+    for (int t = tid; t < T; t += Sh::THREADS) {
+        const size_t th = (size_t)(b * T + t) * H + h;
+        s_sc[8 * t + 0] = sigmoid_f32(a.b_raw[th]);
+        float alpha_h = 1.f;
+        if (GATE == KDA_GATE_PER_HEAD) alpha_h = expf(gate_log_decay(a.g_raw[th] + (a.dt_bias ? a.dt_bias[h] : 0.f), rate, a.gp));
+        s_sc[8 * t + 2] = alpha_h;
+    }
+    __syncthreads();
+    for (int t = warp; t < T; t += NWARPS) {             // one warp per token
+        float kk = 0.f, qq = 0.f, kq = 0.f;
+        for (int c = lane; c < D; c += 32) {
+            const float kc = s_k[t * D + c], qc = s_q[t * D + c];
+            kk = fmaf(kc, kc, kk);
+            qq = fmaf(qc, qc, qq);
+            kq = fmaf(kc, qc, kq);
+        }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             kk += __shfl_xor_sync(0xffffffffu, kk, off);
@@ -143,44 +156,39 @@ recurrent_kernel(const RecArgs a)
             kq += __shfl_xor_sync(0xffffffffu, kq, off);
         }
         if (lane == 0) {
-            s_red[0][warp] = kk;
-            s_red[1][warp] = qq;
-            s_red[2][warp] = kq;
+            const float rk = 1.0f / sqrtf(kk + a.gp.l2_eps);
+            const float rq = a.gp.scale / sqrtf(qq + a.gp.l2_eps);
+            s_sc[8 * t + 1] = kq * rk * rq;
+            s_sc[8 * t + 3] = rk;
+            s_sc[8 * t + 4] = rq;
         }
-        __syncthreads();
-        kk = 0.f; qq = 0.f; kq = 0.f;
-#pragma unroll
-        for (int w = 0; w < NWARPS; ++w) {
-            kk += s_red[0][w];
-            qq += s_red[1][w];
-            kq += s_red[2][w];
-        }
-        const float rk = 1.0f / sqrtf(kk + a.gp.l2_eps);
-        const float rq = a.gp.scale / sqrtf(qq + a.gp.l2_eps);
-        const float qk = kq * rk * rq;
-        const float beta = sigmoid_f32(a.b_raw[(size_t)tok * H + h]);
-        float alpha_h = 1.f;
-        if (GATE == KDA_GATE_PER_HEAD) {
-            const float x = a.g_raw[(size_t)tok * H + h] + (a.dt_bias ? a.dt_bias[h] : 0.f);
-            alpha_h = expf(gate_log_decay(x, rate, a.gp));
-        }
-        if (tid < D) {
-            s_k[tid] = kc * rk;
-            s_q[tid] = qc * rq;
-        }
-        __syncthreads();
+    }
+    __syncthreads();
+    for (int e = tid; e < T * D; e += Sh::THREADS) {
+        const int t = e / D;
+        s_k[e] *= s_sc[8 * t + 3];
+        s_q[e] *= s_sc[8 * t + 4];
+    }
+    __syncthreads();
+
+    for (int t = 0; t < T; ++t) {
+        const int64_t tok = b * T + t;
+        const size_t rowbase = ((size_t)tok * H + h) * D;
+        const float beta = s_sc[8 * t + 0];
+        const float qk = s_sc[8 * t + 1];
+        const float alpha_h = s_sc[8 * t + 2];
 
         // ---- per-lane column constants --------------------------------------------------------
         float kh[CPL], qh[CPL], al[CPL];
 #pragma unroll
         for (int j = 0; j < NV4; ++j) {
-            const int c = 4 * (li + LPR * j);
+            const int c = t * D + 4 * (li + LPR * j);
             const float4 k4 = *reinterpret_cast<const float4*>(&s_k[c]);
             const float4 q4 = *reinterpret_cast<const float4*>(&s_q[c]);
             kh[4 * j + 0] = k4.x; kh[4 * j + 1] = k4.y; kh[4 * j + 2] = k4.z; kh[4 * j + 3] = k4.w;
             qh[4 * j + 0] = q4.x; qh[4 * j + 1] = q4.y; qh[4 * j + 2] = q4.z; qh[4 * j + 3] = q4.w;
             if (GATE == KDA_GATE_PER_CHANNEL) {
-                const float4 a4 = *reinterpret_cast<const float4*>(&s_alpha[c]);
+                const float4 a4 = *reinterpret_cast<const float4*>(&s_al[c]);
                 al[4 * j + 0] = a4.x; al[4 * j + 1] = a4.y; al[4 * j + 2] = a4.z; al[4 * j + 3] = a4.w;
             } else {
                 al[4 * j + 0] = al[4 * j + 1] = al[4 * j + 2] = al[4 * j + 3] = alpha_h;
@@ -191,7 +199,7 @@ recurrent_kernel(const RecArgs a)
 #pragma unroll
         for (int s = 0; s < STEPS; ++s) {
             const int row = warp * Sh::ROWS_PER_WARP + s * RPS + row_in_step;
-            const float vj = to_f32(vp[rowbase + row]);
+            const float vj = s_v[t * D + row];
             float pk = 0.f, pq = 0.f;
 #pragma unroll
             for (int j = 0; j < NV4; ++j) {
@@ -226,16 +234,24 @@ recurrent_kernel(const RecArgs a)
 #pragma unroll
             for (int j = 0; j < NV4; ++j) __stcs(d4 + li + LPR * j, st[s][j]);
         }
-        if (VERIFY) __syncthreads();  // the next token rewrites the shared column constants
     }
 }
+
+// Dynamic shared memory of one recurrent CTA: four [T][D] tiles and 8 scalars per token.
+inline size_t recurrent_smem_bytes(int D, int T) { return sizeof(float) * ((size_t)4 * T * D + 8 * (size_t)T); }
 
 template <int D, int GATE, bool VERIFY, typename TIn, typename TOut>
 cudaError_t launch_t(const RecArgs& a, int64_t batch, cudaStream_t stream)
 {
     const int64_t blocks = batch * a.H;
     if (blocks <= 0) return cudaSuccess;
-    recurrent_kernel<D, GATE, VERIFY, TIn, TOut><<<(unsigned)blocks, RecShape<D>::THREADS, 0, stream>>>(a);
+    const size_t smem = recurrent_smem_bytes(D, VERIFY ? a.t_draft : 1);
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(recurrent_kernel<D, GATE, VERIFY, TIn, TOut>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    recurrent_kernel<D, GATE, VERIFY, TIn, TOut><<<(unsigned)blocks, RecShape<D>::THREADS, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
