@@ -172,6 +172,44 @@ int32_t kda_recurrent_verify(const kda_params* p,
                              kda_stream_t stream);
 
 /*
+ * kda_chunk_prefill that also keeps the state at every chunk boundary, the snapshots a prefix
+ * cache stores ("linear_attention", section "两种计算形态": the state h at each chunk boundary is
+ * materialised; section "prefix cache 与投机解码").
+ *   chunk_states   device fp32 [num_chunks][H][D][D] (transposed like the pool), where chunk
+ *                  c = seq_chunk_offset(i) + m is chunk m of sequence i, seq_chunk_offset(i) =
+ *                  sum_{j<i} ceil(len_j / chunk_size), num_chunks = seq_chunk_offset(num_seqs).
+ *                  Entry c holds the state after chunk c (prefix length (m + 1) * chunk_size,
+ *                  or the whole sequence for its last chunk).  Padding rows write nothing.
+ *   chunk_states_capacity  number of [H][D][D] entries the buffer holds; a table that needs more
+ *                  entries is recorded as device error 2 and the extra snapshots are dropped.
+ * Everything else is as kda_chunk_prefill.
+ */
+int32_t kda_chunk_prefill_snapshots(const kda_params* p,
+                                    const void* q, const void* k, const void* v,
+                                    const float* g_raw, const float* b_raw,
+                                    const float* A_log, const float* dt_bias,
+                                    const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                                    float* state_pool, int64_t num_slots, const int32_t* state_idx,
+                                    void* out,
+                                    void* workspace, size_t workspace_bytes,
+                                    float* chunk_states, int64_t chunk_states_capacity,
+                                    kda_stream_t stream);
+
+/*
+ * Commit accepted drafts after kda_recurrent_verify ("linear_attention", section "prefix cache 与
+ * 投机解码": after acceptance the intermediate state of the accepted length is scattered back to
+ * the pool).  For request b with a = accept_len[b] (device int32 [batch]): 1 <= a <= t_draft copies
+ * inter_states[b][a - 1] into state_pool[state_idx[b]]; a = 0 leaves the slot unchanged; a padding
+ * row (state_idx < 0) is skipped.  An accept_len outside [0, t_draft] or a slot >= num_slots is
+ * skipped and recorded as device error 4 or 1.  The buffers may not overlap.
+ */
+int32_t kda_commit_verified_states(const kda_params* p,
+                                   const float* inter_states, int32_t batch, int32_t t_draft,
+                                   const int32_t* accept_len,
+                                   float* state_pool, int64_t num_slots, const int32_t* state_idx,
+                                   kda_stream_t stream);
+
+/*
  * kda_chunk_prefill for callers that cannot allocate device memory.  The pages have no
  * counterpart to this entry point; it exists for the library's users.
  *
@@ -209,8 +247,9 @@ int32_t kda_chunk_prefill_static_scratch(const kda_params* p,
 
 /*
  * Synchronise `stream`, then read and clear the device error word that the kernels set when
- * they meet an out-of-range state_idx (code 1), a malformed cu_seqlens (code 2) or a bounded
- * wait inside a kernel that gave up (code 3; that call's results are invalid).  *code receives
+ * they meet an out-of-range state_idx (code 1), a malformed cu_seqlens or a snapshot table too
+ * small for it (code 2), a bounded wait inside a kernel that gave up (code 3; that call's
+ * results are invalid) or an accept_len outside [0, t_draft] (code 4).  *code receives
  * the first recorded code (0 when none) for the current device.  Returns KDA_OK when no error was
  * recorded, KDA_ERR_DEVICE_CHECK when one was, KDA_ERR_CUDA when the synchronisation failed.
  */

@@ -8,6 +8,7 @@ from .binding import (  # noqa: F401
     Params,
     chunk_prefill,
     check_device_errors,
+    commit_verified_states,
     lib,
     make_params,
     prefill_workspace_size,

@@ -85,6 +85,11 @@ def lib() -> ctypes.CDLL:
         L.kda_recurrent_verify.argtypes = [ctypes.POINTER(Params), _P, _P, _P, _P, _P, _P, _P,
                                            ctypes.c_int32, ctypes.c_int32, _P, ctypes.c_int64, _P,
                                            _P, _P, _P]
+        L.kda_chunk_prefill_snapshots.restype = ctypes.c_int32
+        L.kda_chunk_prefill_snapshots.argtypes = L.kda_chunk_prefill.argtypes[:-1] + [_P, ctypes.c_int64, _P]
+        L.kda_commit_verified_states.restype = ctypes.c_int32
+        L.kda_commit_verified_states.argtypes = [ctypes.POINTER(Params), _P, ctypes.c_int32, ctypes.c_int32, _P,
+                                                 _P, ctypes.c_int64, _P, _P]
         L.kda_check_device_errors.restype = ctypes.c_int32
         L.kda_check_device_errors.argtypes = [_P, ctypes.POINTER(ctypes.c_int32)]
         _lib = L
@@ -161,11 +166,13 @@ PREFILL_PHASES = ("chunk_table", "chunk_intra", "chunk_state")
 
 def chunk_prefill(q, k, v, g_raw, b_raw, A_log, dt_bias, cu_seqlens, state_pool, state_idx,
                   out=None, *, params: Params | None = None, workspace=None, stream=None,
-                  events=None, **kw):
+                  events=None, chunk_states=None, **kw):
     """kda_chunk_prefill on torch tensors; returns ``out`` ([T, H, D]).  ``state_pool`` is
     updated in place.  ``kw`` are forwarded to :func:`make_params` when ``params`` is None.
     With ``events`` (4 recorded-once ``torch.cuda.Event``), kda_chunk_prefill_timed records them
-    around the chunk-table, intra-chunk and state-pass kernels."""
+    around the chunk-table, intra-chunk and state-pass kernels.  With ``chunk_states``
+    ([num_chunks, H, D, D] fp32), kda_chunk_prefill_snapshots also writes the state after every
+    chunk (chunks numbered by sequence, then position)."""
     T, H, D = q.shape
     if params is None:
         params = make_params(H, D, io_dtype=q.dtype, **kw)
@@ -190,6 +197,13 @@ def chunk_prefill(q, k, v, g_raw, b_raw, A_log, dt_bias, cu_seqlens, state_pool,
     args = (ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(b_raw), _ptr(A_log),
             _ptr(dt_bias), _ptr(cu_seqlens), n, T, _ptr(state_pool), state_pool.shape[0], _ptr(state_idx),
             _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    if chunk_states is not None:
+        if events is not None:
+            raise ValueError("events and chunk_states cannot be combined")
+        _dev(chunk_states, "chunk_states", torch.float32)
+        rc = lib().kda_chunk_prefill_snapshots(*args[:-1], _ptr(chunk_states), chunk_states.shape[0], args[-1])
+        _check(rc, "kda_chunk_prefill_snapshots")
+        return out
     if events is None:
         rc = lib().kda_chunk_prefill(*args)
     else:
@@ -253,6 +267,22 @@ def recurrent_verify(q, k, v, g_raw, b_raw, A_log, dt_bias, state_pool, state_id
                                     _ptr(inter), _ptr(out), _stream(stream))
     _check(rc, "kda_recurrent_verify")
     return out, inter
+
+
+def commit_verified_states(inter, accept_len, state_pool, state_idx, *, params: Params | None = None,
+                           stream=None, **kw):
+    """kda_commit_verified_states: copy inter[b, accept_len[b] - 1] into each accepted slot."""
+    B, Td, H, D, _ = inter.shape
+    if params is None:
+        params = make_params(H, D, **kw)
+    _dev(inter, "inter", torch.float32)
+    _dev(accept_len, "accept_len", torch.int32)
+    _dev(state_pool, "state_pool", torch.float32)
+    _dev(state_idx, "state_idx", torch.int32)
+    rc = lib().kda_commit_verified_states(ctypes.byref(params), _ptr(inter), B, Td, _ptr(accept_len),
+                                          _ptr(state_pool), state_pool.shape[0], _ptr(state_idx), _stream(stream))
+    _check(rc, "kda_commit_verified_states")
+    return state_pool
 
 
 def check_device_errors(stream=None) -> int:

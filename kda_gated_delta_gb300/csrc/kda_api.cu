@@ -90,7 +90,8 @@ int32_t prefill_impl(const kda_params* p, const void* q, const void* k, const vo
                      const float* dt_bias, const int32_t* cu_seqlens, int32_t num_seqs,
                      int64_t total_tokens, float* state_pool, int64_t num_slots,
                      const int32_t* state_idx, void* out, void* workspace,
-                     size_t workspace_bytes, kda_stream_t stream, const cudaEvent_t* events)
+                     size_t workspace_bytes, kda_stream_t stream, const cudaEvent_t* events,
+                     float* chunk_states = nullptr, int64_t chunk_states_capacity = 0)
 {
     if (num_seqs < 0) return KDA_ERR_INVALID_ARG;
     int32_t rc = check_common(p, q, k, v, g_raw, b_raw, A_log, dt_bias, total_tokens, state_pool,
@@ -105,7 +106,8 @@ int32_t prefill_impl(const kda_params* p, const void* q, const void* k, const vo
         return KDA_ERR_WORKSPACE;
     return from_cuda(kda::launch_prefill(*p, gate_params(*p), q, k, v, g_raw, b_raw, A_log, dt_bias,
                                          cu_seqlens, num_seqs, total_tokens, state_pool, num_slots,
-                                         state_idx, out, workspace, (cudaStream_t)stream, events));
+                                         state_idx, out, workspace, (cudaStream_t)stream, events,
+                                         chunk_states, chunk_states_capacity));
 }
 }  // namespace
 
@@ -133,6 +135,35 @@ int32_t kda_chunk_prefill_timed(const kda_params* p, const void* q, const void* 
     return prefill_impl(p, q, k, v, g_raw, b_raw, A_log, dt_bias, cu_seqlens, num_seqs, total_tokens,
                         state_pool, num_slots, state_idx, out, workspace, workspace_bytes, stream,
                         reinterpret_cast<const cudaEvent_t*>(events));
+}
+
+int32_t kda_chunk_prefill_snapshots(const kda_params* p, const void* q, const void* k, const void* v,
+                                    const float* g_raw, const float* b_raw, const float* A_log,
+                                    const float* dt_bias, const int32_t* cu_seqlens, int32_t num_seqs,
+                                    int64_t total_tokens, float* state_pool, int64_t num_slots,
+                                    const int32_t* state_idx, void* out, void* workspace,
+                                    size_t workspace_bytes, float* chunk_states,
+                                    int64_t chunk_states_capacity, kda_stream_t stream)
+{
+    if (!chunk_states || chunk_states_capacity < 0) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(chunk_states)) return KDA_ERR_MISALIGNED;
+    return prefill_impl(p, q, k, v, g_raw, b_raw, A_log, dt_bias, cu_seqlens, num_seqs, total_tokens,
+                        state_pool, num_slots, state_idx, out, workspace, workspace_bytes, stream, nullptr,
+                        chunk_states, chunk_states_capacity);
+}
+
+int32_t kda_commit_verified_states(const kda_params* p, const float* inter_states, int32_t batch,
+                                   int32_t t_draft, const int32_t* accept_len, float* state_pool,
+                                   int64_t num_slots, const int32_t* state_idx, kda_stream_t stream)
+{
+    if (!p || batch < 0 || t_draft < 1 || t_draft > 16 || num_slots < 0 || p->num_heads <= 0)
+        return KDA_ERR_INVALID_ARG;
+    if (!kda::recurrent_supported(*p)) return KDA_ERR_UNSUPPORTED;
+    if (batch == 0) return KDA_OK;
+    if (!inter_states || !accept_len || !state_pool || !state_idx) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(inter_states) || !aligned16(state_pool)) return KDA_ERR_MISALIGNED;
+    return from_cuda(kda::launch_commit(p->num_heads, p->head_dim, inter_states, batch, t_draft, accept_len,
+                                        state_pool, num_slots, state_idx, (cudaStream_t)stream));
 }
 
 int32_t kda_recurrent_decode(const kda_params* p, const void* q, const void* k, const void* v,

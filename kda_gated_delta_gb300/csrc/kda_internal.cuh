@@ -16,6 +16,7 @@ enum DeviceError : int32_t {
     kDevErrStateIndex = 1,   // state_idx[i] >= num_slots
     kDevErrSeqlens = 2,      // cu_seqlens not non-decreasing within [0, T]
     kDevErrTimeout = 3,      // a bounded wait inside a kernel gave up (the call's results are invalid)
+    kDevErrAcceptLen = 4,    // accept_len outside [0, t_draft]
 };
 
 // Scalar parameters every kernel needs, resolved on the host from kda_params.
@@ -65,6 +66,9 @@ cudaError_t launch_recurrent(const kda_params& p, const GateParams& gp, const vo
                              const int32_t* state_idx, void* out, cudaStream_t stream);
 bool recurrent_supported(const kda_params& p);
 cudaError_t recurrent_read_and_clear_error(int32_t* code);
+cudaError_t launch_commit(int H, int D, const float* inter, int32_t batch, int32_t t_draft,
+                          const int32_t* accept_len, float* pool, int64_t num_slots,
+                          const int32_t* state_idx, cudaStream_t stream);
 
 size_t prefill_workspace_bytes(const kda_params& p, int32_t num_seqs, int64_t total_tokens);
 cudaError_t launch_prefill(const kda_params& p, const GateParams& gp, const void* q,
@@ -73,7 +77,8 @@ cudaError_t launch_prefill(const kda_params& p, const GateParams& gp, const void
                            int32_t num_seqs, int64_t total_tokens, float* pool,
                            int64_t num_slots, const int32_t* state_idx, void* out,
                            void* workspace, cudaStream_t stream,
-                           const cudaEvent_t* events = nullptr);
+                           const cudaEvent_t* events = nullptr,
+                           float* chunk_states = nullptr, int64_t chunk_states_capacity = 0);
 bool prefill_supported(const kda_params& p);
 cudaError_t prefill_read_and_clear_error(int32_t* code);
 

@@ -509,6 +509,8 @@ struct StateArgs {
     const float* ws;
     size_t ws_stride;
     void* out;
+    float* snap;           // optional chunk-boundary states [chunks][H][D][D]
+    int64_t snap_cap;      // entries in snap
 };
 
 template <int C, int D, int NV>
@@ -658,6 +660,17 @@ __global__ void __launch_bounds__(256, 1) chunk_state_kernel(const StateArgs a)
             __syncthreads();  // every thread has finished reading the old S
 #pragma unroll
             for (int i = 0; i < CPT; ++i) s_S[(tr + TR * i) * NV + tv] = acc[i];
+        }
+        if (a.snap) {                                // state after this chunk
+            __syncthreads();
+            if (ch < a.snap_cap) {
+                for (int e = tid; e < D * NV; e += THREADS) {
+                    const int v = e / D, c = e % D;
+                    a.snap[(((size_t)ch * H + h) * D + v0 + v) * D + c] = s_S[c * NV + v];
+                }
+            } else if (tid == 0) {
+                record_error(kDevErrSeqlens);
+            }
         }
     }
     __syncthreads();
@@ -897,6 +910,16 @@ __global__ void __launch_bounds__(128, 1) chunk_state_tc_kernel(const StateArgs 
                     if (r0 + j < L) out[((size_t)(t0 + r0 + j) * H + h) * D + tid] = from_f32<TOut>(o[j]);
             }
             tc::tmem_wait_st();
+            if (a.snap) {                            // state after this chunk
+                if (ch < a.snap_cap) {
+                    float* Sd = a.snap + (((size_t)ch * H + h) * D + tid) * (size_t)D;
+#pragma unroll
+                    for (int c = 0; c < D; c += 4)
+                        *reinterpret_cast<float4*>(Sd + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+                } else if (tid == 0) {
+                    record_error(kDevErrSeqlens);
+                }
+            }
         }
         tc::tc_fence_before();
         __syncthreads();
@@ -1415,7 +1438,7 @@ cudaError_t run_prefill(const kda_params& p, const GateParams& gp, const void* q
                         const void* v, const float* g_raw, const float* b_raw, const float* A_log,
                         const float* dt_bias, const int32_t* cu, int32_t N, int64_t T, float* pool,
                         int64_t num_slots, const int32_t* state_idx, void* out, void* workspace,
-                        cudaStream_t stream, const cudaEvent_t* ev)
+                        cudaStream_t stream, const cudaEvent_t* ev, float* snap, int64_t snap_cap)
 {
     const int H = p.num_heads;
     const WsLayout w = ws_layout(C, D, H, N, T);
@@ -1465,6 +1488,7 @@ cudaError_t run_prefill(const kda_params& p, const GateParams& gp, const void* q
     sa.chunk_start = chunk_start; sa.chunk_len = chunk_len; sa.seq_off = seq_off; sa.cu = cu;
     sa.state_idx = state_idx; sa.pool = pool; sa.num_slots = num_slots; sa.max_chunks = w.max_chunks;
     sa.T = T; sa.N = N; sa.H = H; sa.ws = ws; sa.ws_stride = w.per_chunk_head; sa.out = out;
+    sa.snap = snap; sa.snap_cap = snap_cap;
     if constexpr (kTensorCore) {
         auto state = chunk_state_tc_kernel<TOut>;
         e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmemBytes);
@@ -1490,9 +1514,9 @@ cudaError_t dispatch_dtypes(const kda_params& p, const GateParams& gp, const voi
                             const void* v, const float* g_raw, const float* b_raw, const float* A_log,
                             const float* dt_bias, const int32_t* cu, int32_t N, int64_t T, float* pool,
                             int64_t num_slots, const int32_t* state_idx, void* out, void* ws,
-                            cudaStream_t s, const cudaEvent_t* ev)
+                            cudaStream_t s, const cudaEvent_t* ev, float* snap, int64_t snap_cap)
 {
-#define KDA_RUN(TI, TO) run_prefill<C, D, TI, TO>(p, gp, q, k, v, g_raw, b_raw, A_log, dt_bias, cu, N, T, pool, num_slots, state_idx, out, ws, s, ev)
+#define KDA_RUN(TI, TO) run_prefill<C, D, TI, TO>(p, gp, q, k, v, g_raw, b_raw, A_log, dt_bias, cu, N, T, pool, num_slots, state_idx, out, ws, s, ev, snap, snap_cap)
     if (p.io_dtype == KDA_BF16) {
         if (p.out_dtype == KDA_BF16) return KDA_RUN(__nv_bfloat16, __nv_bfloat16);
         return KDA_RUN(__nv_bfloat16, float);
@@ -1523,13 +1547,15 @@ cudaError_t launch_prefill(const kda_params& p, const GateParams& gp, const void
                            const float* A_log, const float* dt_bias, const int32_t* cu_seqlens,
                            int32_t num_seqs, int64_t total_tokens, float* pool,
                            int64_t num_slots, const int32_t* state_idx, void* out,
-                           void* workspace, cudaStream_t stream, const cudaEvent_t* events)
+                           void* workspace, cudaStream_t stream, const cudaEvent_t* events,
+                           float* chunk_states, int64_t chunk_states_capacity)
 {
 #define KDA_DIM(CC, DD)                                                                            \
     if (p.chunk_size == CC && p.head_dim == DD)                                                    \
         return dispatch_dtypes<CC, DD>(p, gp, q, k, v, g_raw, b_raw, A_log, dt_bias, cu_seqlens,  \
                                        num_seqs, total_tokens, pool, num_slots, state_idx, out,    \
-                                       workspace, stream, events);
+                                       workspace, stream, events, chunk_states,                    \
+                                       chunk_states_capacity);
     KDA_DIM(16, 16) KDA_DIM(16, 32) KDA_DIM(16, 64) KDA_DIM(16, 128)
     KDA_DIM(32, 16) KDA_DIM(32, 32) KDA_DIM(32, 64) KDA_DIM(32, 128)
     KDA_DIM(64, 16) KDA_DIM(64, 32) KDA_DIM(64, 64) KDA_DIM(64, 128)

@@ -311,6 +311,45 @@ cudaError_t launch_recurrent(const kda_params& p, const GateParams& gp, const vo
     return dispatch_dim<false>(p, a, batch, stream);
 }
 
+namespace {
+// One CTA of 256 threads per (request, head): copy the accepted draft's state into the pool slot.
+__global__ void __launch_bounds__(256) commit_kernel(const float* __restrict__ inter, int32_t t_draft,
+                                                     const int32_t* __restrict__ accept_len, float* pool,
+                                                     int64_t num_slots, const int32_t* __restrict__ state_idx,
+                                                     int H, int D)
+{
+    const int64_t bh = blockIdx.x;
+    const int64_t b = bh / H;
+    const int h = (int)(bh - b * H);
+    const int64_t slot = state_idx[b];
+    if (slot < 0) return;
+    if (slot >= num_slots) {
+        if (threadIdx.x == 0 && h == 0) record_error(kDevErrStateIndex);
+        return;
+    }
+    const int acc = accept_len[b];
+    if (acc < 0 || acc > t_draft) {
+        if (threadIdx.x == 0 && h == 0) record_error(kDevErrAcceptLen);
+        return;
+    }
+    if (acc == 0) return;
+    const size_t n4 = (size_t)D * D / 4;
+    const float4* src = reinterpret_cast<const float4*>(inter + (((size_t)b * t_draft + acc - 1) * H + h) * (size_t)D * D);
+    float4* dst = reinterpret_cast<float4*>(pool + ((size_t)slot * H + h) * (size_t)D * D);
+    for (size_t i = threadIdx.x; i < n4; i += blockDim.x) __stcs(dst + i, __ldcs(src + i));
+}
+}  // namespace
+
+cudaError_t launch_commit(int H, int D, const float* inter, int32_t batch, int32_t t_draft,
+                          const int32_t* accept_len, float* pool, int64_t num_slots,
+                          const int32_t* state_idx, cudaStream_t stream)
+{
+    const int64_t blocks = (int64_t)batch * H;
+    if (blocks <= 0) return cudaSuccess;
+    commit_kernel<<<(unsigned)blocks, 256, 0, stream>>>(inter, t_draft, accept_len, pool, num_slots, state_idx, H, D);
+    return cudaGetLastError();
+}
+
 cudaError_t recurrent_read_and_clear_error(int32_t* code)
 {
     int32_t zero = 0;
