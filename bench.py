@@ -81,6 +81,17 @@ def decode_bytes(B, H, D, io_bytes, out_bytes):
     return B * H * (2 * D * D * 4 + 3 * D * io_bytes + D * 4 + 4 + D * out_bytes) + H * 4 + H * D * 4
 
 
+def replay_bytes(write_pos, ring_len, H, D, io_bytes, out_bytes):
+    """Bytes of one buffered-decode step: checkpoint read, ring entries read (d, k, a), then either
+    the ring append (non-flush) or the checkpoint write (flush), plus the token's inputs/output."""
+    total = 0
+    for wp in write_pos:
+        per = D * D * 4 + wp * 3 * D * 4 + 3 * D * io_bytes + D * 4 + 4 + D * out_bytes
+        per += D * D * 4 if wp == ring_len - 1 else 3 * D * 4
+        total += H * per
+    return total + H * 4 + H * D * 4
+
+
 def verify_bytes(B, Td, H, D, io_bytes, out_bytes, per_head_gate=True):
     g = 4 if per_head_gate else D * 4
     per_token = D * D * 4 + 3 * D * io_bytes + g + 4 + D * out_bytes    # inter-state write + inputs + out
@@ -298,16 +309,24 @@ def run_ours(args):
     out_dec = torch.empty(wd.batch, H, D, dtype=torch.bfloat16, device=dev)
     out_ver = torch.empty(wv.batch * wv.t_draft, H, D, dtype=torch.bfloat16, device=dev)
     inter = torch.empty(wv.batch, wv.t_draft, H, D, D, dtype=torch.float32, device=dev)
+    # buffered (ReplaySSM) decode on the decode workload: ring length 8 (the length the pages'
+    # microbenchmark used), cursors staggered across requests so 1/8 of the rows flush per step
+    RL = 8
+    rpool = dec["pool"].clone()
+    rings = kda.replay_rings(rpool.shape[0], H, D, RL, device=dev)
+    rpos = [torch.tensor([(t + b) % RL for b in range(wd.batch)], dtype=torch.int32, device=dev) for t in range(RL)]
+    out_rep = torch.empty(wd.batch, H, D, dtype=torch.bfloat16, device=dev)
 
     K, W = args.steps, args.warmup
     ev = lambda: torch.cuda.Event(enable_timing=True)
     pre_ev = [[ev() for _ in range(4)] for _ in range(K + W)]
     dec_ev = [[ev(), ev()] for _ in range(K + W)]
     ver_ev = [[ev(), ev()] for _ in range(K + W)]
+    rep_ev = [[ev(), ev()] for _ in range(K + W)]
     for e in [x for row in pre_ev for x in row]:
         e.record()          # create the underlying CUDA events before handing them to the library
     torch.cuda.synchronize()
-    launches_per_step = 3 + 1 + 1
+    launches_per_step = 3 + 1 + 1 + 1
 
     def step(i):
         kda.chunk_prefill(pre["q"], pre["k"], pre["v"], pre["g_raw"], pre["b_raw"], pre["A_log"],
@@ -322,6 +341,10 @@ def run_ours(args):
                              ver["dt_bias"], ver["pool"], ver["state_idx"], wv.t_draft, inter, out_ver,
                              params=p_ver)
         ver_ev[i][1].record()
+        rep_ev[i][0].record()
+        kda.replay_decode(dec["q"], dec["k"], dec["v"], dec["g_raw"], dec["b_raw"], dec["A_log"], dec["dt_bias"],
+                          rpool, dec["state_idx"], rings, rpos[i % RL], None, out_rep, params=p_dec)
+        rep_ev[i][1].record()
 
     for i in range(W):
         step(K + i)
@@ -353,6 +376,7 @@ def run_ours(args):
     pre_ms = reduce_max(dist, sum(phase_ms), dev)
     dec_ms = reduce_max(dist, sum(dec_ev[i][0].elapsed_time(dec_ev[i][1]) for i in range(K)) / K, dev)
     ver_ms = reduce_max(dist, sum(ver_ev[i][0].elapsed_time(ver_ev[i][1]) for i in range(K)) / K, dev)
+    rep_ms = reduce_max(dist, sum(rep_ev[i][0].elapsed_time(rep_ev[i][1]) for i in range(K)) / K, dev)
 
     pre_B = prefill_bytes(T, Np, H, D, 2, 2)
     dec_B = decode_bytes(wd.batch, H, D, 2, 2)
@@ -360,6 +384,8 @@ def run_ours(args):
     value = world * T / (pre_ms * 1e-3)
     dec_value = world * wd.batch / (dec_ms * 1e-3)
     ver_value = world * wv.batch * wv.t_draft / (ver_ms * 1e-3)
+    rep_B = sum(replay_bytes(rpos[i % RL].tolist(), RL, H, D, 2, 2) for i in range(K)) / K
+    rep_value = world * wd.batch / (rep_ms * 1e-3)
 
     def roof(bytes_, ms, kernels_):
         ach = bytes_ / (ms * 1e-3) / 1e9
@@ -372,7 +398,8 @@ def run_ours(args):
     kernels = [{"name": n, "ms": round(m, 5)} for n, m in
                zip(("kda_chunk_table", "kda_chunk_intra", "kda_chunk_state"), phase_ms)]
     kernels += [{"name": "kda_recurrent_decode", "ms": round(dec_ms, 5)},
-                {"name": "kda_recurrent_verify", "ms": round(ver_ms, 5)}]
+                {"name": "kda_recurrent_verify", "ms": round(ver_ms, 5)},
+                {"name": "kda_replay_decode", "ms": round(rep_ms, 5)}]
     tot = sum(k["ms"] for k in kernels)
     for k in kernels:
         k["share"] = round(k["ms"] / tot, 4)
@@ -436,6 +463,10 @@ def run_ours(args):
         "verify": {"value": round(ver_value, 1), "unit": UNIT, "ms": round(ver_ms, 5),
                    "roofline": roof(ver_B, ver_ms, ("kda_recurrent_verify",)),
                    "workload": "gdn_verify_bf16: 64 requests x 4 drafts, per-head gate, inter states"},
+        "decode_replay": {"value": round(rep_value, 1), "unit": UNIT, "ms": round(rep_ms, 5), "ring_len": RL,
+                          "roofline": roof(rep_B, rep_ms, ("kda_replay_decode",)),
+                          "workload": "decode_bf16 through the buffered decode: ring 8, cursors staggered, "
+                                      "1/8 of the rows flush per step (averaged over the timed steps)"},
         "kernels": kernels,
         "clocks": clk,
         "e2e": e2e,

@@ -154,6 +154,38 @@ int32_t kda_recurrent_decode(const kda_params* p,
                              kda_stream_t stream);
 
 /*
+ * Buffered single-token decode ("ReplaySSM -- buffered output-only decode", sections 2, 3 and 5):
+ * the slot's state is kept as a checkpoint in state_pool plus a ring of the steps taken since,
+ * and the state before the current token is rebuilt as
+ *     S = Diag(prod_j a_j) S_checkpoint + sum_j (k_j o prod_{i>j} a_i)^T d_j   (j < write_pos[b])
+ * The token then takes the same decode step as kda_recurrent_decode (its output is that of the
+ * plain recurrence).  A non-flush step appends (d, k_hat, a) of this token at ring position
+ * write_pos[b] and leaves the checkpoint untouched; a flush step (write_pos[b] == ring_len - 1,
+ * or force_flush[b] != 0) writes the new state into the checkpoint instead.  The caller then
+ * advances the cursor of the slot: 0 after a flush, write_pos + 1 otherwise; a new or copied slot
+ * starts at 0 (an empty ring).
+ *   ring_d   device fp32 [num_slots][H][ring_len][D]   corrected deltas d = beta (v - v_hat)
+ *   ring_k   device fp32 [num_slots][H][ring_len][D]   normalised keys
+ *   ring_a   device fp32 [num_slots][H][ring_len][D] (per-channel gate) or
+ *            [num_slots][H][ring_len] (per-head gate)    decays a = e^{g} (not g: products of
+ *            factors <= 1 keep the rebuild exact to fp32 rounding)
+ *   write_pos  device int32 [batch] in [0, ring_len); outside it the row is treated as padding
+ *            and recorded as device error 5.  force_flush: device int32 [batch] or NULL.
+ *   1 <= ring_len <= 32.  With ring_len = 1 every step flushes and the call computes exactly
+ *   what kda_recurrent_decode computes.
+ */
+int32_t kda_replay_decode(const kda_params* p,
+                          const void* q, const void* k, const void* v,
+                          const float* g_raw, const float* b_raw,
+                          const float* A_log, const float* dt_bias,
+                          int32_t batch,
+                          float* state_pool, int64_t num_slots, const int32_t* state_idx,
+                          float* ring_d, float* ring_k, float* ring_a, int32_t ring_len,
+                          const int32_t* write_pos, const int32_t* force_flush,
+                          void* out,
+                          kda_stream_t stream);
+
+/*
  * Multi-token verify ("PR #26888 report": target_verify with disable_state_update and an
  * intermediate-state buffer; "linear_attention", section "prefix cache 与投机解码").
  * Request b owns tokens b*t_draft .. b*t_draft + t_draft - 1 of the inputs (request-major).
@@ -249,7 +281,8 @@ int32_t kda_chunk_prefill_static_scratch(const kda_params* p,
  * Synchronise `stream`, then read and clear the device error word that the kernels set when
  * they meet an out-of-range state_idx (code 1), a malformed cu_seqlens or a snapshot table too
  * small for it (code 2), a bounded wait inside a kernel that gave up (code 3; that call's
- * results are invalid) or an accept_len outside [0, t_draft] (code 4).  *code receives
+ * results are invalid), an accept_len outside [0, t_draft] (code 4) or a replay write_pos
+ * outside [0, ring_len) (code 5).  *code receives
  * the first recorded code (0 when none) for the current device.  Returns KDA_OK when no error was
  * recorded, KDA_ERR_DEVICE_CHECK when one was, KDA_ERR_CUDA when the synchronisation failed.
  */

@@ -14,5 +14,7 @@ from .binding import (  # noqa: F401
     prefill_workspace_size,
     recurrent_decode,
     recurrent_verify,
+    replay_decode,
+    replay_rings,
     status_string,
 )

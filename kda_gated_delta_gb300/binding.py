@@ -87,6 +87,9 @@ def lib() -> ctypes.CDLL:
                                            _P, _P, _P]
         L.kda_chunk_prefill_snapshots.restype = ctypes.c_int32
         L.kda_chunk_prefill_snapshots.argtypes = L.kda_chunk_prefill.argtypes[:-1] + [_P, ctypes.c_int64, _P]
+        L.kda_replay_decode.restype = ctypes.c_int32
+        L.kda_replay_decode.argtypes = [ctypes.POINTER(Params), _P, _P, _P, _P, _P, _P, _P, ctypes.c_int32,
+                                        _P, ctypes.c_int64, _P, _P, _P, _P, ctypes.c_int32, _P, _P, _P, _P]
         L.kda_commit_verified_states.restype = ctypes.c_int32
         L.kda_commit_verified_states.argtypes = [ctypes.POINTER(Params), _P, ctypes.c_int32, ctypes.c_int32, _P,
                                                  _P, ctypes.c_int64, _P, _P]
@@ -267,6 +270,42 @@ def recurrent_verify(q, k, v, g_raw, b_raw, A_log, dt_bias, state_pool, state_id
                                     _ptr(inter), _ptr(out), _stream(stream))
     _check(rc, "kda_recurrent_verify")
     return out, inter
+
+
+def replay_rings(num_slots, num_heads, head_dim, ring_len, gate="kda", device="cuda"):
+    """Allocate zeroed ReplaySSM rings (d, k, a) for kda_replay_decode."""
+    d = torch.zeros(num_slots, num_heads, ring_len, head_dim, device=device)
+    k = torch.zeros_like(d)
+    a = torch.zeros_like(d) if gate == "kda" else torch.zeros(num_slots, num_heads, ring_len, device=device)
+    return d, k, a
+
+
+def replay_decode(q, k, v, g_raw, b_raw, A_log, dt_bias, state_pool, state_idx, rings, write_pos,
+                  force_flush=None, out=None, *, params: Params | None = None, stream=None, **kw):
+    """kda_replay_decode: one token per request against checkpoint + ring.  ``rings`` is the
+    (ring_d, ring_k, ring_a) triple; ``write_pos`` [B] int32 is not advanced here."""
+    B, H, D = q.shape
+    ring_d, ring_k, ring_a = rings
+    if params is None:
+        params = make_params(H, D, io_dtype=q.dtype, **kw)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _dev(t, name, q.dtype)
+    for name, t in (("g_raw", g_raw), ("b_raw", b_raw), ("A_log", A_log), ("dt_bias", dt_bias),
+                    ("state_pool", state_pool), ("ring_d", ring_d), ("ring_k", ring_k), ("ring_a", ring_a)):
+        _dev(t, name, torch.float32)
+    _dev(state_idx, "state_idx", torch.int32)
+    _dev(write_pos, "write_pos", torch.int32)
+    _dev(force_flush, "force_flush", torch.int32)
+    if out is None:
+        out = torch.empty((B, H, D), device=q.device,
+                          dtype=torch.float32 if params.out_dtype == KDA_F32 else torch.bfloat16)
+    _dev(out, "out")
+    rc = lib().kda_replay_decode(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(b_raw),
+                                 _ptr(A_log), _ptr(dt_bias), B, _ptr(state_pool), state_pool.shape[0],
+                                 _ptr(state_idx), _ptr(ring_d), _ptr(ring_k), _ptr(ring_a), ring_d.shape[2],
+                                 _ptr(write_pos), _ptr(force_flush), _ptr(out), _stream(stream))
+    _check(rc, "kda_replay_decode")
+    return out
 
 
 def commit_verified_states(inter, accept_len, state_pool, state_idx, *, params: Params | None = None,

@@ -183,6 +183,26 @@ int32_t kda_recurrent_decode(const kda_params* p, const void* q, const void* k, 
                                            state_idx, out, (cudaStream_t)stream));
 }
 
+int32_t kda_replay_decode(const kda_params* p, const void* q, const void* k, const void* v,
+                          const float* g_raw, const float* b_raw, const float* A_log,
+                          const float* dt_bias, int32_t batch, float* state_pool, int64_t num_slots,
+                          const int32_t* state_idx, float* ring_d, float* ring_k, float* ring_a,
+                          int32_t ring_len, const int32_t* write_pos, const int32_t* force_flush,
+                          void* out, kda_stream_t stream)
+{
+    if (batch < 0 || ring_len < 1 || ring_len > 32) return KDA_ERR_INVALID_ARG;
+    int32_t rc = check_common(p, q, k, v, g_raw, b_raw, A_log, dt_bias, batch, state_pool,
+                              num_slots, state_idx, out);
+    if (rc != KDA_OK) return rc;
+    if (!kda::recurrent_supported(*p)) return KDA_ERR_UNSUPPORTED;
+    if (batch == 0) return KDA_OK;
+    if (!ring_d || !ring_k || !ring_a || !write_pos) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(ring_d) || !aligned16(ring_k) || !aligned16(ring_a)) return KDA_ERR_MISALIGNED;
+    return from_cuda(kda::launch_replay(*p, gate_params(*p), q, k, v, g_raw, b_raw, A_log, dt_bias, batch,
+                                        state_pool, num_slots, state_idx, ring_d, ring_k, ring_a, ring_len,
+                                        write_pos, force_flush, out, (cudaStream_t)stream));
+}
+
 int32_t kda_recurrent_verify(const kda_params* p, const void* q, const void* k, const void* v,
                              const float* g_raw, const float* b_raw, const float* A_log,
                              const float* dt_bias, int32_t batch, int32_t t_draft,

@@ -17,6 +17,7 @@ enum DeviceError : int32_t {
     kDevErrSeqlens = 2,      // cu_seqlens not non-decreasing within [0, T]
     kDevErrTimeout = 3,      // a bounded wait inside a kernel gave up (the call's results are invalid)
     kDevErrAcceptLen = 4,    // accept_len outside [0, t_draft]
+    kDevErrWritePos = 5,     // replay write_pos outside [0, ring_len)
 };
 
 // Scalar parameters every kernel needs, resolved on the host from kda_params.
@@ -66,6 +67,12 @@ cudaError_t launch_recurrent(const kda_params& p, const GateParams& gp, const vo
                              const int32_t* state_idx, void* out, cudaStream_t stream);
 bool recurrent_supported(const kda_params& p);
 cudaError_t recurrent_read_and_clear_error(int32_t* code);
+cudaError_t launch_replay(const kda_params& p, const GateParams& gp, const void* q, const void* k,
+                          const void* v, const float* g_raw, const float* b_raw, const float* A_log,
+                          const float* dt_bias, int32_t batch, float* pool, int64_t num_slots,
+                          const int32_t* state_idx, float* ring_d, float* ring_k, float* ring_a,
+                          int32_t ring_len, const int32_t* write_pos, const int32_t* force_flush,
+                          void* out, cudaStream_t stream);
 cudaError_t launch_commit(int H, int D, const float* inter, int32_t batch, int32_t t_draft,
                           const int32_t* accept_len, float* pool, int64_t num_slots,
                           const int32_t* state_idx, cudaStream_t stream);

@@ -48,7 +48,16 @@ struct RecArgs {
     int H;
     int t_draft;
     GateParams gp;
+    // replay mode: per-slot rings of the last steps since the checkpoint (see kda_replay_decode)
+    float* ring_d;            // [slots][H][L][D] corrected deltas
+    float* ring_k;            // [slots][H][L][D] normalised keys
+    float* ring_a;            // [slots][H][L][D] (per-channel) or [slots][H][L] (per-head) decays
+    int ring_len;             // L
+    const int32_t* write_pos; // [batch] entries committed in the ring (0 .. L-1)
+    const int32_t* force_flush;  // [batch] or null
 };
+
+enum { kModeDecode = 0, kModeVerify = 1, kModeReplay = 2 };
 
 template <int D>
 struct RecShape {
@@ -64,9 +73,11 @@ struct RecShape {
     static_assert(NWARPS * ROWS_PER_WARP == D, "rows");
 };
 
-// GATE: KDA_GATE_PER_CHANNEL or KDA_GATE_PER_HEAD.  VERIFY: write every intermediate state to
-// `inter` and leave the pool untouched; otherwise update the pool slot in place (t_draft = 1).
-template <int D, int GATE, bool VERIFY, typename TIn, typename TOut>
+// GATE: KDA_GATE_PER_CHANNEL or KDA_GATE_PER_HEAD.  MODE: kModeDecode updates the pool slot in
+// place; kModeVerify writes every intermediate state to `inter` and leaves the pool untouched;
+// kModeReplay rebuilds the state from the slot's checkpoint and ring, then either appends this
+// step to the ring or (flush) writes the new state to the checkpoint.
+template <int D, int GATE, int MODE, typename TIn, typename TOut>
 __global__ void __launch_bounds__(RecShape<D>::THREADS, (D >= 128 ? 2 : 4))
 recurrent_kernel(const RecArgs a)
 {
@@ -81,12 +92,23 @@ recurrent_kernel(const RecArgs a)
     const int64_t bh = blockIdx.x;
     const int64_t b = bh / H;
     const int h = (int)(bh - b * H);
+    constexpr bool VERIFY = MODE == kModeVerify;
     const int T = VERIFY ? a.t_draft : 1;
 
     int64_t slot = a.state_idx[b];
     if (slot >= a.num_slots) {
         if (tid == 0) record_error(kDevErrStateIndex);
         slot = -1;
+    }
+    int wp = 0;
+    bool flush = false;
+    if (MODE == kModeReplay && slot >= 0) {
+        wp = a.write_pos[b];
+        if (wp < 0 || wp >= a.ring_len) {
+            if (tid == 0) record_error(kDevErrWritePos);
+            slot = -1;
+        }
+        flush = wp == a.ring_len - 1 || (a.force_flush && a.force_flush[b] != 0);
     }
     TOut* out = reinterpret_cast<TOut*>(a.out);
     if (slot < 0) {  // padding row: zero outputs, no state traffic
@@ -169,6 +191,62 @@ recurrent_kernel(const RecArgs a)
         s_k[e] *= s_sc[8 * t + 3];
         s_q[e] *= s_sc[8 * t + 4];
     }
+    if (MODE == kModeReplay && wp > 0) {
+        // S = Diag(prod_j a_j) S0 + sum_j d_j^T (k_j o prod_{i>j} a_i) over the wp committed steps
+        // (ReplaySSM, section 3.11): stage the ring, turn k_j into k_j o prod_{i>j} a_i in place
+        float* s_rk = s_sc + 8 * T;               // [L][D]
+        float* s_rd = s_rk + a.ring_len * D;      // [L][D]
+        float* s_ra = s_rd + a.ring_len * D;      // [L][D] (per-channel) or [L]
+        float* s_tot = s_ra + a.ring_len * D;     // [D]
+        const size_t rb = ((size_t)slot * H + h) * (size_t)a.ring_len;
+        // stage the committed entries with 16-byte loads (all issued before any is used)
+        const float4* gk = reinterpret_cast<const float4*>(a.ring_k + rb * D);
+        const float4* gd = reinterpret_cast<const float4*>(a.ring_d + rb * D);
+        const float4* ga = reinterpret_cast<const float4*>(a.ring_a + rb * D);
+        for (int e = tid; e < wp * D / 4; e += Sh::THREADS) {
+            const float4 k4 = __ldcs(gk + e), d4 = __ldcs(gd + e);
+            float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (GATE == KDA_GATE_PER_CHANNEL) a4 = __ldcs(ga + e);
+            reinterpret_cast<float4*>(s_rk)[e] = k4;
+            reinterpret_cast<float4*>(s_rd)[e] = d4;
+            if (GATE == KDA_GATE_PER_CHANNEL) reinterpret_cast<float4*>(s_ra)[e] = a4;
+        }
+        if (GATE == KDA_GATE_PER_HEAD)
+            for (int j = tid; j < wp; j += Sh::THREADS) s_ra[j] = a.ring_a[rb + j];
+        __syncthreads();
+        for (int c = tid; c < D; c += Sh::THREADS) {
+            float pr = 1.f;
+            for (int j = wp - 1; j >= 0; --j) {
+                s_rk[j * D + c] *= pr;
+                pr *= (GATE == KDA_GATE_PER_CHANNEL) ? s_ra[j * D + c] : s_ra[j];
+            }
+            s_tot[c] = pr;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int s = 0; s < STEPS; ++s)
+#pragma unroll
+            for (int j4 = 0; j4 < NV4; ++j4) {
+                const float4 tt = *reinterpret_cast<const float4*>(&s_tot[4 * (li + LPR * j4)]);
+                st[s][j4] = make_float4(st[s][j4].x * tt.x, st[s][j4].y * tt.y, st[s][j4].z * tt.z, st[s][j4].w * tt.w);
+            }
+        for (int j = 0; j < wp; ++j) {                 // one ring entry: CPL keys x STEPS deltas per lane
+            float4 kw[NV4];
+            float dj[STEPS];
+#pragma unroll
+            for (int j4 = 0; j4 < NV4; ++j4) kw[j4] = *reinterpret_cast<const float4*>(&s_rk[j * D + 4 * (li + LPR * j4)]);
+#pragma unroll
+            for (int s = 0; s < STEPS; ++s) dj[s] = s_rd[j * D + warp * Sh::ROWS_PER_WARP + s * RPS + row_in_step];
+#pragma unroll
+            for (int s = 0; s < STEPS; ++s)
+#pragma unroll
+                for (int j4 = 0; j4 < NV4; ++j4) {
+                    float4& e = st[s][j4];
+                    e.x = fmaf(dj[s], kw[j4].x, e.x); e.y = fmaf(dj[s], kw[j4].y, e.y);
+                    e.z = fmaf(dj[s], kw[j4].z, e.z); e.w = fmaf(dj[s], kw[j4].w, e.w);
+                }
+        }
+    }
     __syncthreads();
 
     for (int t = 0; t < T; ++t) {
@@ -224,6 +302,10 @@ recurrent_kernel(const RecArgs a)
                 e.z = fmaf(delta, kh[4 * j + 2], e.z); e.w = fmaf(delta, kh[4 * j + 3], e.w);
             }
             if (li == 0) out[rowbase + row] = from_f32<TOut>(o);
+            if (MODE == kModeReplay && !flush) {      // append d to the ring; the state stays put
+                if (li == 0) a.ring_d[(((size_t)slot * H + h) * a.ring_len + wp) * D + row] = delta;
+                continue;
+            }
             float* dst;
             if (VERIFY) {
                 dst = a.inter + ((((size_t)b * T + t) * H + h) * (size_t)D + row) * D;
@@ -234,53 +316,65 @@ recurrent_kernel(const RecArgs a)
 #pragma unroll
             for (int j = 0; j < NV4; ++j) __stcs(d4 + li + LPR * j, st[s][j]);
         }
+        if (MODE == kModeReplay && !flush) {          // append k_hat and the decay of this step
+            const size_t re = ((size_t)slot * H + h) * a.ring_len + wp;
+            for (int c = tid; c < D; c += Sh::THREADS) {
+                a.ring_k[re * D + c] = s_k[c];
+                if (GATE == KDA_GATE_PER_CHANNEL) a.ring_a[re * D + c] = s_al[c];
+            }
+            if (GATE == KDA_GATE_PER_HEAD && tid == 0) a.ring_a[re] = alpha_h;
+        }
     }
 }
 
-// Dynamic shared memory of one recurrent CTA: four [T][D] tiles and 8 scalars per token.
-inline size_t recurrent_smem_bytes(int D, int T) { return sizeof(float) * ((size_t)4 * T * D + 8 * (size_t)T); }
+// Dynamic shared memory of one recurrent CTA: four [T][D] tiles and 8 scalars per token, plus in
+// replay mode three [L][D] ring tiles and one [D] vector.
+inline size_t recurrent_smem_bytes(int D, int T, int L)
+{
+    return sizeof(float) * ((size_t)4 * T * D + 8 * (size_t)T + (size_t)3 * L * D + D);
+}
 
-template <int D, int GATE, bool VERIFY, typename TIn, typename TOut>
+template <int D, int GATE, int MODE, typename TIn, typename TOut>
 cudaError_t launch_t(const RecArgs& a, int64_t batch, cudaStream_t stream)
 {
     const int64_t blocks = batch * a.H;
     if (blocks <= 0) return cudaSuccess;
-    const size_t smem = recurrent_smem_bytes(D, VERIFY ? a.t_draft : 1);
+    const size_t smem = recurrent_smem_bytes(D, MODE == kModeVerify ? a.t_draft : 1, MODE == kModeReplay ? a.ring_len : 0);
     if (smem > 48 * 1024) {
-        const cudaError_t e = cudaFuncSetAttribute(recurrent_kernel<D, GATE, VERIFY, TIn, TOut>,
+        const cudaError_t e = cudaFuncSetAttribute(recurrent_kernel<D, GATE, MODE, TIn, TOut>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    recurrent_kernel<D, GATE, VERIFY, TIn, TOut><<<(unsigned)blocks, RecShape<D>::THREADS, smem, stream>>>(a);
+    recurrent_kernel<D, GATE, MODE, TIn, TOut><<<(unsigned)blocks, RecShape<D>::THREADS, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
-template <int D, int GATE, bool VERIFY>
+template <int D, int GATE, int MODE>
 cudaError_t dispatch_dtypes(const kda_params& p, const RecArgs& a, int64_t batch, cudaStream_t s)
 {
     if (p.io_dtype == KDA_BF16) {
-        if (p.out_dtype == KDA_BF16) return launch_t<D, GATE, VERIFY, __nv_bfloat16, __nv_bfloat16>(a, batch, s);
-        return launch_t<D, GATE, VERIFY, __nv_bfloat16, float>(a, batch, s);
+        if (p.out_dtype == KDA_BF16) return launch_t<D, GATE, MODE, __nv_bfloat16, __nv_bfloat16>(a, batch, s);
+        return launch_t<D, GATE, MODE, __nv_bfloat16, float>(a, batch, s);
     }
-    if (p.out_dtype == KDA_BF16) return launch_t<D, GATE, VERIFY, float, __nv_bfloat16>(a, batch, s);
-    return launch_t<D, GATE, VERIFY, float, float>(a, batch, s);
+    if (p.out_dtype == KDA_BF16) return launch_t<D, GATE, MODE, float, __nv_bfloat16>(a, batch, s);
+    return launch_t<D, GATE, MODE, float, float>(a, batch, s);
 }
 
-template <int D, bool VERIFY>
+template <int D, int MODE>
 cudaError_t dispatch_gate(const kda_params& p, const RecArgs& a, int64_t batch, cudaStream_t s)
 {
-    if (p.gate_kind == KDA_GATE_PER_HEAD) return dispatch_dtypes<D, KDA_GATE_PER_HEAD, VERIFY>(p, a, batch, s);
-    return dispatch_dtypes<D, KDA_GATE_PER_CHANNEL, VERIFY>(p, a, batch, s);
+    if (p.gate_kind == KDA_GATE_PER_HEAD) return dispatch_dtypes<D, KDA_GATE_PER_HEAD, MODE>(p, a, batch, s);
+    return dispatch_dtypes<D, KDA_GATE_PER_CHANNEL, MODE>(p, a, batch, s);
 }
 
-template <bool VERIFY>
+template <int MODE>
 cudaError_t dispatch_dim(const kda_params& p, const RecArgs& a, int64_t batch, cudaStream_t s)
 {
     switch (p.head_dim) {
-    case 16: return dispatch_gate<16, VERIFY>(p, a, batch, s);
-    case 32: return dispatch_gate<32, VERIFY>(p, a, batch, s);
-    case 64: return dispatch_gate<64, VERIFY>(p, a, batch, s);
-    case 128: return dispatch_gate<128, VERIFY>(p, a, batch, s);
+    case 16: return dispatch_gate<16, MODE>(p, a, batch, s);
+    case 32: return dispatch_gate<32, MODE>(p, a, batch, s);
+    case 64: return dispatch_gate<64, MODE>(p, a, batch, s);
+    case 128: return dispatch_gate<128, MODE>(p, a, batch, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -307,8 +401,25 @@ cudaError_t launch_recurrent(const kda_params& p, const GateParams& gp, const vo
     a.q = q; a.k = k; a.v = v; a.g_raw = g_raw; a.b_raw = b_raw; a.A_log = A_log; a.dt_bias = dt_bias;
     a.pool_in = pool_in; a.pool_out = pool_out; a.inter = inter; a.state_idx = state_idx; a.out = out;
     a.num_slots = num_slots; a.H = p.num_heads; a.t_draft = t_draft; a.gp = gp;
-    if (inter != nullptr) return dispatch_dim<true>(p, a, batch, stream);
-    return dispatch_dim<false>(p, a, batch, stream);
+    a.ring_d = a.ring_k = a.ring_a = nullptr; a.ring_len = 0; a.write_pos = nullptr; a.force_flush = nullptr;
+    if (inter != nullptr) return dispatch_dim<kModeVerify>(p, a, batch, stream);
+    return dispatch_dim<kModeDecode>(p, a, batch, stream);
+}
+
+cudaError_t launch_replay(const kda_params& p, const GateParams& gp, const void* q, const void* k,
+                          const void* v, const float* g_raw, const float* b_raw, const float* A_log,
+                          const float* dt_bias, int32_t batch, float* pool, int64_t num_slots,
+                          const int32_t* state_idx, float* ring_d, float* ring_k, float* ring_a,
+                          int32_t ring_len, const int32_t* write_pos, const int32_t* force_flush,
+                          void* out, cudaStream_t stream)
+{
+    RecArgs a;
+    a.q = q; a.k = k; a.v = v; a.g_raw = g_raw; a.b_raw = b_raw; a.A_log = A_log; a.dt_bias = dt_bias;
+    a.pool_in = pool; a.pool_out = pool; a.inter = nullptr; a.state_idx = state_idx; a.out = out;
+    a.num_slots = num_slots; a.H = p.num_heads; a.t_draft = 1; a.gp = gp;
+    a.ring_d = ring_d; a.ring_k = ring_k; a.ring_a = ring_a; a.ring_len = ring_len;
+    a.write_pos = write_pos; a.force_flush = force_flush;
+    return dispatch_dim<kModeReplay>(p, a, batch, stream);
 }
 
 namespace {
