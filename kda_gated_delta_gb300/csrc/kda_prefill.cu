@@ -707,7 +707,7 @@ struct TcBars {
     uint64_t mma_c;                   // (a), (b2), (c), (b) complete
     uint64_t drain;                   // used once, to drain the tensor core after a failed wait
 };
-constexpr size_t kTcSmemBytes = kSmBars + 256;
+constexpr size_t kTcSmemBytes = kSmBars + 1024;
 static_assert(kTcSmemBytes <= 232448, "state-pass shared memory");
 
 // TMEM column map (512 columns allocated; each accumulator starts at a multiple of its width)
@@ -820,6 +820,21 @@ __global__ void __launch_bounds__(128, 1) chunk_state_tc_kernel(const StateArgs 
     constexpr uint32_t kId64 = tc::idesc_tf32(128, 64), kId128 = tc::idesc_tf32(128, 128);
     bool ok = true;
 
+    float* s_gl = reinterpret_cast<float*>(sm + kSmBars + sizeof(TcBars) + 32);  // e^{G_L} of the chunk
+    int64_t prev_t0 = 0;
+    int prev_L = 0;
+    // O^T of the previous chunk -> out (read in the next chunk, off the serial chain)
+    auto write_out = [&](int64_t t0o, int Lo) {
+#pragma unroll
+        for (int r0 = 0; r0 < C; r0 += 16) {
+            float o[16];
+            tc::tmem_ld16(tmem + lane + kT_OUT + r0, o);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (r0 + j < Lo) out[((size_t)(t0o + r0 + j) * H + h) * D + tid] = from_f32<TOut>(o[j]);
+        }
+    };
+
     for (int64_t ch = c_begin; ch < c_end; ++ch) {
         const uint32_t i = (uint32_t)(ch - c_begin);
         const uint32_t ph = i & 1u, b = i & 1u, phb = (i >> 1) & 1u;
@@ -840,8 +855,9 @@ __global__ void __launch_bounds__(128, 1) chunk_state_tc_kernel(const StateArgs 
             tc::mma_commit(&bars->mma_a);
             if (!ok) *s_abort = 1;
         }
-        // Delta^T = U^T - S^T W^T, rounded copy to TMEM; decay S^T by e^{G_L}
+        // output of the previous chunk; then Delta^T = U^T - S^T W^T, rounded copy to TMEM
         {
+            if (i > 0) write_out(prev_t0, prev_L);
             const bool okw = tc::mbar_wait(&bars->ug[b], phb, kWaitPolls) && tc::mbar_wait(&bars->mma_a, ph, kWaitPolls);
             if (!okw) *s_abort = 1;
             if (okw && tid == 0) landed(&bars->ug[b]);
@@ -854,9 +870,8 @@ __global__ void __launch_bounds__(128, 1) chunk_state_tc_kernel(const StateArgs 
                 for (int j = 0; j < 16; ++j) d[j] = tc::round_tf32(sU[(r0 + j) * D + tid] - d[j]);
                 tc::tmem_st16_nowait(tmem + lane + kT_DOP + r0, d);
             }
+            s_gl[tid] = sG[tid];                     // the buffer is refilled before (c) retires
             tc::tmem_wait_st();
-#pragma unroll
-            for (int c = 0; c < D; ++c) S[c] *= sG[c];
         }
         tc::tc_fence_before();
         __syncthreads();
@@ -886,7 +901,7 @@ __global__ void __launch_bounds__(128, 1) chunk_state_tc_kernel(const StateArgs 
             tc::mma_commit(&bars->mma_c);
             if (!ok) *s_abort = 1;
         }
-        // S^T += Delta^T Ktil; refresh the tf32 copy; write O
+        // S^T <- S^T Diag(e^{G_L}) + Delta^T Ktil; refresh the tf32 copy
         {
             if (!tc::mbar_wait(&bars->mma_c, ph, kWaitPolls)) *s_abort = 1;
             tc::tc_fence_after();
@@ -896,18 +911,10 @@ __global__ void __launch_bounds__(128, 1) chunk_state_tc_kernel(const StateArgs 
                 tc::tmem_ld16(tmem + lane + kT_SC + c, d);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    S[c + j] += d[j];
+                    S[c + j] = fmaf(S[c + j], s_gl[c + j], d[j]);
                     d[j] = tc::round_tf32(S[c + j]);
                 }
                 tc::tmem_st16_nowait(tmem + lane + kT_SOP + c, d);
-            }
-#pragma unroll
-            for (int r0 = 0; r0 < C; r0 += 16) {
-                float o[16];
-                tc::tmem_ld16(tmem + lane + kT_OUT + r0, o);
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    if (r0 + j < L) out[((size_t)(t0 + r0 + j) * H + h) * D + tid] = from_f32<TOut>(o[j]);
             }
             tc::tmem_wait_st();
             if (a.snap) {                            // state after this chunk
@@ -921,6 +928,8 @@ __global__ void __launch_bounds__(128, 1) chunk_state_tc_kernel(const StateArgs 
                 }
             }
         }
+        prev_t0 = t0;
+        prev_L = L;
         tc::tc_fence_before();
         __syncthreads();
         if (*s_abort) break;
@@ -930,6 +939,10 @@ __global__ void __launch_bounds__(128, 1) chunk_state_tc_kernel(const StateArgs 
             load(&bars->kt, TcRec::KT, TcRec::KT, 32768, ch + 1);
             load(&bars->qb, TcRec::QB, TcRec::QB, 32768, ch + 1);
         }
+    }
+    if (!*s_abort) {
+        tc::tc_fence_after();
+        write_out(prev_t0, prev_L);                  // the last chunk's output
     }
 
     if (*s_abort) {
@@ -982,7 +995,9 @@ constexpr uint32_t R1_BYTES = 96 * D * 4;
 constexpr uint32_t OFF_T = OFF_R1;                              // T = (I + A)^{-1}     [C][LDA]
 constexpr uint32_t OFF_IT = OFF_R1 + C * LDA * 4;               // T image (rows r, K = j)
 constexpr uint32_t OFF_BP = OFF_R1 + R1_BYTES;                  // block products       [NB][D]
-constexpr uint32_t OFF_X = OFF_BP + NB * D * 4;                 // 3 scratch 16 x 16 blocks
+constexpr uint32_t OFF_EB = OFF_BP + NB * D * 4;                // prod of block products before  [NB][D]
+constexpr uint32_t OFF_EA = OFF_EB + NB * D * 4;                // prod of block products after   [NB][D]
+constexpr uint32_t OFF_X = OFF_EA + NB * D * 4;                 // 3 scratch 16 x 16 blocks
 constexpr uint32_t OFF_BETA = OFF_X + 3 * 256 * 4;              // beta                 [C]
 constexpr uint32_t OFF_V = OFF_BETA + C * 4;                    // v bf16               [C][D]
 constexpr uint32_t OFF_BAR = OFF_V + C * D * 2;                 // 2 mbarriers
@@ -1056,6 +1071,8 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
     float* sIT = reinterpret_cast<float*>(sm + OFF_IT);
     float* sBp = reinterpret_cast<float*>(sm + OFF_BP);
     float* sX = reinterpret_cast<float*>(sm + OFF_X);
+    float* sEb = reinterpret_cast<float*>(sm + OFF_EB);
+    float* sEa = reinterpret_cast<float*>(sm + OFF_EA);
     float* sBeta = reinterpret_cast<float*>(sm + OFF_BETA);
     uint64_t* bar_g = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     uint64_t* bar_uw = bar_g + 1;
@@ -1223,6 +1240,11 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
 
     const uint32_t tmem = *s_tmem;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    if (tid < D) {                                  // e^{G} at the block starts / after the block ends
+        const float b0 = sBp[tid], b1 = sBp[D + tid], b2 = sBp[2 * D + tid], b3 = sBp[3 * D + tid];
+        sEb[tid] = 1.f; sEb[D + tid] = b0; sEb[2 * D + tid] = b0 * b1; sEb[3 * D + tid] = (b0 * b1) * b2;
+        sEa[3 * D + tid] = 1.f; sEa[2 * D + tid] = b3; sEa[D + tid] = b3 * b2; sEa[tid] = (b3 * b2) * b1;
+    }
 
     // 4a. Gram operands: B image rows n = 32 (I - 1) + {0..15: k o Rin, 16..31: q o Rin} of row block I;
     //     TMEM lane m <- key j decayed to the start of block I: (k o Rout)[j] * prod_{J < bb < I} bp[bb]
@@ -1275,24 +1297,16 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
     float* wP = reinterpret_cast<float*>(rec + TcRec::P);
     for (int f = tid; f < C * D / 4; f += THREADS) {          // Qbar: rows r, K = c
         const int core = f >> 3, rr = (core >> 5) * 8 + (f & 7), c = (core & 31) * 4;
-        float4 v = ld4(sQ + rr * LD + c);
-        for (int bb = 0; bb < (rr >> 4); ++bb) v = mul4(v, ld4(sBp + bb * D + c));
-        st4(wQ + 4 * f, rnd4(v));
+        st4(wQ + 4 * f, rnd4(mul4(ld4(sQ + rr * LD + c), ld4(sEb + (rr >> 4) * D + c))));
     }
     for (int f = tid; f < C * D / 4; f += THREADS) {          // Ktil^T: rows c, K = r
         const int core = f >> 3, cc = (core >> 4) * 8 + (f & 7), r0 = (core & 15) * 4;
-        float ea = 1.f;
-        for (int bb = (r0 >> 4) + 1; bb < NB; ++bb) ea *= sBp[bb * D + cc];
+        const float ea = sEa[(r0 >> 4) * D + cc];
         const float4 v = make_float4(sAl[r0 * LD + cc] * ea, sAl[(r0 + 1) * LD + cc] * ea,
                                      sAl[(r0 + 2) * LD + cc] * ea, sAl[(r0 + 3) * LD + cc] * ea);
         st4(wKT + 4 * f, rnd4(v));
     }
-    if (tid < D) {
-        float gL = 1.f;
-#pragma unroll
-        for (int bb = 0; bb < NB; ++bb) gL *= sBp[bb * D + tid];
-        wG[tid] = gL;
-    }
+    if (tid < D) wG[tid] = sEb[3 * D + tid] * sBp[3 * D + tid];
     // 4b. Gram result -> off-diagonal blocks of A and P
     if (warp < 3) {
         const bool done = tc::mbar_wait(bar_g, 0, kWaitPolls);
@@ -1343,24 +1357,34 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
         for (int i = 0; i < 16; ++i) sT[(16 * I + i) * LDA + j] = col[i];
     }
     __syncthreads();
-    // 6. off-diagonal blocks of T
-    for (int d = 1; d < NB; ++d) {
-        const int nb = NB - d;
+    // 6. off-diagonal blocks of T, by block distance d (loops unrolled so the loads issue together)
+    auto tblocks = [&](auto dc) {
+        constexpr int d = decltype(dc)::value;
+        constexpr int nb = NB - d;
         for (int e = tid; e < nb * 256; e += THREADS) {      // X_IJ = sum_{J<=K<I} A_IK T_KJ
             const int J = e >> 8, I = J + d, i = (e >> 4) & 15, jj = e & 15;
+            const float* ar = sA + (16 * I + i) * LDA + 16 * J;
+            const float* tc0 = sT + 16 * J * LDA + 16 * J + jj;
             float acc = 0.f;
-            for (int kk = 16 * J; kk < 16 * I; ++kk) acc = fmaf(sA[(16 * I + i) * LDA + kk], sT[kk * LDA + 16 * J + jj], acc);
+#pragma unroll
+            for (int kk = 0; kk < 16 * d; ++kk) acc = fmaf(ar[kk], tc0[kk * LDA], acc);
             sX[e] = acc;
         }
         __syncthreads();
         for (int e = tid; e < nb * 256; e += THREADS) {      // T_IJ = -T_II X_IJ
             const int J = e >> 8, I = J + d, i = (e >> 4) & 15, jj = e & 15;
+            const float* tr = sT + (16 * I + i) * LDA + 16 * I;
+            const float* xc = sX + (J << 8) + jj;
             float acc = 0.f;
-            for (int kk = 0; kk <= i; ++kk) acc = fmaf(sT[(16 * I + i) * LDA + 16 * I + kk], sX[(J << 8) + kk * 16 + jj], acc);
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) acc = kk <= i ? fmaf(tr[kk], xc[kk * 16], acc) : acc;
             sT[(16 * I + i) * LDA + 16 * J + jj] = -acc;
         }
         __syncthreads();
-    }
+    };
+    tblocks(std::integral_constant<int, 1>{});
+    tblocks(std::integral_constant<int, 2>{});
+    tblocks(std::integral_constant<int, 3>{});
 
     // 7. operand images: T (rows r, K = j), (beta V)^T (rows v, K = j), (beta Kbar)^T (rows c, K = j)
     float* sIV = reinterpret_cast<float*>(sm + OFF_IV);
@@ -1374,8 +1398,7 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
         float4 vv, kb;
         float* pv = &vv.x;
         float* pk = &kb.x;
-        float eb = 1.f;
-        for (int bb = 0; bb < (j0 >> 4); ++bb) eb *= sBp[bb * D + row];
+        const float eb = sEb[(j0 >> 4) * D + row];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int j = j0 + i;
