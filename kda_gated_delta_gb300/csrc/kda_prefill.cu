@@ -1104,7 +1104,6 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
         tc::mbar_init(bar_uw, 1);
         tc::fence_mbar_init();
     }
-
     // 1. loads, all issued before any is used (rows past the chunk end: k = q = v = 0, alpha = 1,
     //    beta = 0); thread e handles 8 elements of k, q, v and 4 + 4 of g in rows e >> 4 and (e >> 4) + 32
     __nv_bfloat16* sV = reinterpret_cast<__nv_bfloat16*>(sm + OFF_V);
@@ -1178,33 +1177,58 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
     __syncthreads();
 
     // 2. diagonal sub-blocks: thread (row j, column group cg), columns 4 cg + 32 m.  A warp holds
-    //    rows j = 4w .. 4w + 3, so rows r below the warp's first j are skipped uniformly.
+    //    rows j = 4w .. 4w + 3, so rows r below the warp's first j are skipped uniformly.  The
+    //    per-thread partial sums of all 16 rows are reduced over the 8 column-group lanes at the
+    //    end with one transposed reduction (each lane ends with 4 of the 32 sums).
     {
         const int j = tid >> 3, cg = tid & 7, blk0 = j & ~15;
         const int rstart = (j & 15) & ~3;
         float4 kd[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) kd[m] = ld4(sK + j * LD + 4 * cg + 32 * m);
+        float red[32];                                // [0..15]: A partials, [16..31]: P partials
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) {
+            red[rr] = 0.f;
+            red[16 + rr] = 0.f;
             if (rr < rstart) continue;
             const int r = blk0 + rr;
-            float pa = 0.f, pp = 0.f;
+            float pa[4], pp[4];
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 const int c = 4 * cg + 32 * m;
                 if (r > j) kd[m] = mul4(kd[m], ld4(sAl + r * LD + c));
-                pa = dot4(ld4(sK + r * LD + c), kd[m], pa);
-                pp = dot4(ld4(sQ + r * LD + c), kd[m], pp);
+                pa[m] = dot4(ld4(sK + r * LD + c), kd[m], 0.f);
+                pp[m] = dot4(ld4(sQ + r * LD + c), kd[m], 0.f);
             }
+            red[rr] = (pa[0] + pa[1]) + (pa[2] + pa[3]);
+            red[16 + rr] = (pp[0] + pp[1]) + (pp[2] + pp[3]);
+        }
+        // transposed reduction over the 8 lanes of a row j: 16 + 8 + 4 shuffles
 #pragma unroll
-            for (int off = 4; off > 0; off >>= 1) {
-                pa += __shfl_xor_sync(0xffffffffu, pa, off);
-                pp += __shfl_xor_sync(0xffffffffu, pp, off);
+        for (int lvl = 0; lvl < 3; ++lvl) {
+            const int half = 16 >> lvl, off = 4 >> lvl;
+            const bool upper = (cg & off) != 0;
+#pragma unroll
+            for (int i = 0; i < half; ++i) {
+                const float keep = upper ? red[half + i] : red[i];
+                const float give = upper ? red[i] : red[half + i];
+                red[i] = keep + __shfl_xor_sync(0xffffffffu, give, off);
             }
-            if (cg == 0 && r >= j) {
-                if (r > j) sA[r * LDA + j] = sBeta[r] * pa;
-                sP[r * LDA + j] = pp;
+        }
+        // lane cg now holds the totals of sums 4 cg .. 4 cg + 3
+        const int g = ((cg & 4) ? 4 : 0) + ((cg & 2) ? 2 : 0) + ((cg & 1) ? 1 : 0);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int idx = 4 * g + t;                // 0..31
+            const int rr = idx & 15;
+            const int r = blk0 + rr;
+            if (r >= j) {
+                if (idx < 16) {
+                    if (r > j) sA[r * LDA + j] = sBeta[r] * red[t];
+                } else {
+                    sP[r * LDA + j] = red[t];
+                }
             }
         }
     }
