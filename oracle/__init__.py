@@ -21,6 +21,8 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _BUILD = os.path.join(_HERE, "_build")
 _SO = os.path.join(_BUILD, "libkda_oracle.so")
+# A test can point the wrapper at another build of kda_oracle.c (the mutation test does).
+_SO_OVERRIDE = os.environ.get("KDA_ORACLE_LIB")
 _lock = threading.Lock()
 _lib = None
 
@@ -84,7 +86,7 @@ def lib():
     global _lib
     with _lock:
         if _lib is None:
-            path = build()
+            path = _SO_OVERRIDE or build()
             L = ctypes.CDLL(path)
             L.kdao_softplus.restype = ctypes.c_double
             L.kdao_softplus.argtypes = [ctypes.c_double, ctypes.c_double]

@@ -67,6 +67,19 @@ def test_safe_gate_printed_half_lives():
     assert np.all(g >= -5.0) and np.all(g <= 0.0)
 
 
+def test_safe_gate_slope_grows_with_exp_A():
+    """linear_attention, "实例：Kimi K3": e^A sets the slope of the safe gate's sigmoid; a larger e^A
+    makes the gate more switch-like: for x > 0 the decay moves toward the lower bound, for x < 0
+    toward 0, and at x = 0 it sits at half the lower bound whatever e^A is."""
+    p = oracle.make_params(1, 1, lower_bound=-5.0)
+    A = np.linspace(-2.0, 3.0, 11)
+    pos = [oracle.gate(p, [0.7], None, a)[0] for a in A]
+    neg = [oracle.gate(p, [-0.7], None, a)[0] for a in A]
+    assert all(x > y for x, y in zip(pos, pos[1:]))
+    assert all(x < y for x, y in zip(neg, neg[1:]))
+    assert all(oracle.gate(p, [0.0], None, a)[0] == -2.5 for a in A)
+
+
 def test_l2_normalize():
     x = RNG.normal(size=128)
     y = oracle.l2_normalize(x, eps=0.0)
