@@ -968,50 +968,8 @@ __global__ void __launch_bounds__(128, 1) chunk_state_tc_kernel(const StateArgs 
     }
 }
 
-// ---- intra-chunk kernel for bf16 inputs at C = 64, D = 128 ----------------------------------------
-// One CTA of 512 threads per (chunk, head), writing the tensor-core record (TcRec).
-//   1. loads; alpha = e^{g} (MUFU form of the gate); L2 norms (fused into the loads)
-//   2. diagonal 16 x 16 sub-blocks of A and P: running products of alphas (CUDA cores)
-//   3. per (column, sub-block) products: k o Rin, q o Rin, k o Rout and the block products
-//   4. off-diagonal sub-blocks of A and P on tcgen05, all three row blocks in one MMA: TMEM lane
-//      m holds key j decayed to the start of row block I (m <-> (I, j), 96 rows), the B image holds
-//      the rows of k o Rin and q o Rin of blocks 1..3 (N = 96); only the I(m) = I(n) part is kept
-//   5. Qbar, Ktil^T, P images and e^{G_L} into the record (overlapping the MMA)
-//   6. T = (I + A)^{-1} by blocks: 16 x 16 diagonal blocks by forward substitution, then
-//      T_IJ = -T_II sum_{J<=K<I} A_IK T_KJ
-//   7. tcgen05: U^T = (beta V)^T T^T and W^T = (beta Kbar)^T T^T (M = 128, N = 64, K = 64)
-//   8. U [r][v] and the W image into the record
+// ---- helpers of the bf16 intra-chunk kernel (C = 64, D = 128) -----------------------------------
 namespace itc {
-constexpr int C = 64, D = 128, NB = 4, THREADS = 512;
-constexpr int LD = 132;   // padded row stride (floats) of the [C][D] tiles
-constexpr int LDA = 68;   // padded row stride of the [C][C] tiles
-constexpr uint32_t OFF_K = 0;                                   // k_hat -> k o Rin     [C][LD]
-constexpr uint32_t OFF_Q = OFF_K + C * LD * 4;                  // q_hat -> q o Rin     [C][LD]
-constexpr uint32_t OFF_AL = OFF_Q + C * LD * 4;                 // alpha -> k o Rout    [C][LD]
-constexpr uint32_t OFF_A = OFF_AL + C * LD * 4;                 // A                    [C][LDA]
-constexpr uint32_t OFF_P = OFF_A + C * LDA * 4;                 // P                    [C][LDA]
-constexpr uint32_t OFF_R1 = OFF_P + C * LDA * 4;                // Gram B image, later T and its image
-constexpr uint32_t R1_BYTES = 96 * D * 4;
-constexpr uint32_t OFF_T = OFF_R1;                              // T = (I + A)^{-1}     [C][LDA]
-constexpr uint32_t OFF_IT = OFF_R1 + C * LDA * 4;               // T image (rows r, K = j)
-constexpr uint32_t OFF_BP = OFF_R1 + R1_BYTES;                  // block products       [NB][D]
-constexpr uint32_t OFF_EB = OFF_BP + NB * D * 4;                // prod of block products before  [NB][D]
-constexpr uint32_t OFF_EA = OFF_EB + NB * D * 4;                // prod of block products after   [NB][D]
-constexpr uint32_t OFF_X = OFF_EA + NB * D * 4;                 // 3 scratch 16 x 16 blocks
-constexpr uint32_t OFF_BETA = OFF_X + 3 * 256 * 4;              // beta                 [C]
-constexpr uint32_t OFF_V = OFF_BETA + C * 4;                    // v bf16               [C][D]
-constexpr uint32_t OFF_BAR = OFF_V + C * D * 2;                 // 2 mbarriers
-constexpr uint32_t OFF_TM = OFF_BAR + 16;                       // TMEM base
-constexpr uint32_t BYTES = OFF_TM + 16;
-constexpr uint32_t OFF_IV = OFF_Q;    // (beta V)^T image, rows v, K = j (over q o Rin, free by then)
-constexpr uint32_t OFF_IK = OFF_AL;   // (beta Kbar)^T image, rows c, K = j (over k o Rout)
-static_assert(OFF_IT + C * C * 4 <= OFF_R1 + R1_BYTES, "T and its image fit in R1");
-// TMEM columns (512 allocated)
-constexpr uint32_t T_KD = 0;      // decayed keys, A operand of the Gram MMA (128 cols, lanes 0..95)
-constexpr uint32_t T_G = 128;     // Gram result (96 cols)
-constexpr uint32_t T_U = 256;     // U^T (64)
-constexpr uint32_t T_W = 320;     // W^T (64)
-
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 __device__ __forceinline__ float4 mul4(float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); }
@@ -1056,7 +1014,53 @@ __device__ __forceinline__ void gram_row(int m, int& I, int& j)
 }
 }  // namespace itc
 
-__global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const IntraArgs a)
+// ---- intra-chunk kernel for bf16 inputs at C = 64, D = 128: two CTAs per SM -----------------------
+// One CTA of 256 threads per (chunk, head) with 105 KB of shared memory and 256 TMEM columns, so
+// that two CTAs share an SM and each one's loads, barriers and single-thread MMA issue overlap the
+// other's arithmetic.  Three [C][LD] fp32 tiles hold k_hat, q_hat and alpha; each is reused in
+// place as the pass over it ends.  It writes the tensor-core record (TcRec) that the state pass reads:
+//   1. loads; alpha = e^{g} (MUFU form of the gate); L2 norms fused into the loads
+//   2. diagonal 16 x 16 sub-blocks of A and P by running products of alphas (CUDA cores); each
+//      thread takes key rows j and 15 - j so that all warps do the same number of rows; P goes
+//      straight to the record image, A to a small buffer
+//   3. per (column, sub-block): k o Rout -> Ktil^T record, k o Rin, q o Rin (in place),
+//      (beta Kbar)^T -> TMEM (the thread's TMEM lane is its column)
+//   4. Gram operands in fp16 (kind::f16; same 11-bit significand as tf32, every operand <= 1 in
+//      magnitude): B image = rows of k o Rin and q o Rin of blocks 1..3 (over the q tile), A = key
+//      j decayed to the start of row block I in TMEM (lane m <-> (I, j)); Qbar record
+//   5. while the MMA runs: value loads for (beta V)^T; Gram result -> off-diagonal A and P
+//   6. T = (I + A)^{-1} by blocks (over the alpha tile), then U^T = (beta V)^T T^T and
+//      W^T = (beta Kbar)^T T^T with both A operands in TMEM (kind::tf32)
+namespace itc {
+constexpr int C = 64, D = 128, NB = 4, THREADS = 256;
+constexpr int LD = 132;   // padded row stride (floats) of the [C][D] tiles
+constexpr int LDA = 68;   // padded row stride of the [C][C] tiles
+constexpr uint32_t TILE = C * LD * 4;
+constexpr uint32_t OFF_K = 0;                        // k_hat -> k o Rin; then A and X
+constexpr uint32_t OFF_Q = TILE;                     // q_hat -> q o Rin; then the Gram B image
+constexpr uint32_t OFF_AL = 2 * TILE;                // alpha -> k o Rout; then T and its image
+constexpr uint32_t OFF_AD = 3 * TILE;                // diagonal blocks of A   [NB][16][16]
+constexpr uint32_t OFF_BP = OFF_AD + NB * 256 * 4;   // block products         [NB][D]
+constexpr uint32_t OFF_BETA = OFF_BP + NB * D * 4;   // beta                   [C]
+constexpr uint32_t OFF_BAR = OFF_BETA + C * 4;       // 2 mbarriers
+constexpr uint32_t OFF_TM = OFF_BAR + 16;            // TMEM base
+constexpr uint32_t BYTES = OFF_TM + 16;
+constexpr uint32_t OFF_A = OFF_K;                    // A = sum of diagonal and Gram blocks [C][LDA]
+constexpr uint32_t OFF_X = OFF_K + C * LDA * 4;      // 3 scratch 16 x 16 blocks
+constexpr uint32_t OFF_IB = OFF_Q;                   // Gram B image: 96 rows x 128 fp16
+constexpr uint32_t OFF_T = OFF_AL;                   // T [C][LDA]
+constexpr uint32_t OFF_IT = OFF_AL + C * LDA * 4;    // T image (rows r, K = j), tf32
+static_assert(OFF_X + 3 * 256 * 4 <= OFF_Q, "A and X fit in the k tile");
+static_assert(96 * D * 2 <= TILE, "the fp16 B image fits in the q tile");
+static_assert(OFF_IT + C * C * 4 <= OFF_AD, "T and its image fit in the alpha tile");
+static_assert(2 * (BYTES + 1024) <= 233472, "two CTAs per SM");
+// TMEM columns (256 allocated)
+constexpr uint32_t T_KD = 0;      // decayed keys, fp16 pairs (64 cols); then (beta V)^T (64)
+constexpr uint32_t T_KB = 64;     // (beta Kbar)^T (64)
+constexpr uint32_t T_G = 128;     // Gram result (96); then U^T (64) and W^T (64)
+}  // namespace itc
+
+__global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const IntraArgs a)
 {
     using namespace itc;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -1064,16 +1068,14 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
     float* sK = reinterpret_cast<float*>(sm + OFF_K);
     float* sQ = reinterpret_cast<float*>(sm + OFF_Q);
     float* sAl = reinterpret_cast<float*>(sm + OFF_AL);
+    float* sAD = reinterpret_cast<float*>(sm + OFF_AD);
+    float* sBp = reinterpret_cast<float*>(sm + OFF_BP);
+    float* sBeta = reinterpret_cast<float*>(sm + OFF_BETA);
     float* sA = reinterpret_cast<float*>(sm + OFF_A);
-    float* sP = reinterpret_cast<float*>(sm + OFF_P);
-    float* sB = reinterpret_cast<float*>(sm + OFF_R1);
+    float* sX = reinterpret_cast<float*>(sm + OFF_X);
     float* sT = reinterpret_cast<float*>(sm + OFF_T);
     float* sIT = reinterpret_cast<float*>(sm + OFF_IT);
-    float* sBp = reinterpret_cast<float*>(sm + OFF_BP);
-    float* sX = reinterpret_cast<float*>(sm + OFF_X);
-    float* sEb = reinterpret_cast<float*>(sm + OFF_EB);
-    float* sEa = reinterpret_cast<float*>(sm + OFF_EA);
-    float* sBeta = reinterpret_cast<float*>(sm + OFF_BETA);
+    unsigned char* sIB = sm + OFF_IB;
     uint64_t* bar_g = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     uint64_t* bar_uw = bar_g + 1;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + OFF_TM);
@@ -1095,8 +1097,12 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
     const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(a.q);
     const __nv_bfloat16* vp = reinterpret_cast<const __nv_bfloat16*>(a.v);
 
+    // record fields, addressed from one base pointer where they are written
+    unsigned char* const rec = reinterpret_cast<unsigned char*>(a.ws + ((size_t)ch * H + h) * a.ws_stride);
+#define KDA_REC(field) reinterpret_cast<float*>(rec + TcRec::field)
+
     if (warp == 0) {
-        tc::tmem_alloc(s_tmem, 512);
+        tc::tmem_alloc(s_tmem, 256);
         tc::tmem_relinquish();
     }
     if (tid == 0) {
@@ -1104,35 +1110,36 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
         tc::mbar_init(bar_uw, 1);
         tc::fence_mbar_init();
     }
-    // 1. loads, all issued before any is used (rows past the chunk end: k = q = v = 0, alpha = 1,
-    //    beta = 0); thread e handles 8 elements of k, q, v and 4 + 4 of g in rows e >> 4 and (e >> 4) + 32
-    __nv_bfloat16* sV = reinterpret_cast<__nv_bfloat16*>(sm + OFF_V);
+    // 1. loads, all issued before any is used (rows past the chunk end: k = q = 0, alpha = 1,
+    //    beta = 0).  k, q: 8 elements in rows (tid >> 4) + 16 i; g: 4 elements in rows (tid >> 5) + 8 i
     {
-        uint4 kv[2], qv[2], vv[2];
-        float4 gv[4];
+        uint4 kv[4], qv[4];
+        float4 gv[8];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int e = tid + i * THREADS, r = e >> 4, c8 = (e & 15) * 8;
-            kv[i] = qv[i] = vv[i] = make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < 4; ++i) {
+            const int r = (tid >> 4) + 16 * i, c8 = (tid & 15) * 8;
+            kv[i] = qv[i] = make_uint4(0, 0, 0, 0);
             if (r < L) {
                 const size_t idx = ((size_t)(t0 + r) * H + h) * D + c8;
                 kv[i] = *reinterpret_cast<const uint4*>(kp + idx);
                 qv[i] = *reinterpret_cast<const uint4*>(qp + idx);
-                vv[i] = *reinterpret_cast<const uint4*>(vp + idx);
             }
         }
+        const int c4 = (tid & 31) * 4;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int e = tid + i * THREADS, r = e >> 5, c4 = (e & 31) * 4;
+        for (int i = 0; i < 8; ++i) {
+            const int r = (tid >> 5) + 8 * i;
             gv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (r < L) gv[i] = *reinterpret_cast<const float4*>(a.g_raw + ((size_t)(t0 + r) * H + h) * D + c4);
         }
         float bt = 0.f;
         if (tid < L) bt = a.b_raw[(size_t)(t0 + tid) * H + h];
+        float4 db = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a.dt_bias) db = *reinterpret_cast<const float4*>(a.dt_bias + (size_t)h * D + c4);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 4; ++i) {
             // the 16 consecutive lanes that hold row r reduce its squared norms with shuffles
-            const int e = tid + i * THREADS, r = e >> 4, c8 = (e & 15) * 8;
+            const int r = (tid >> 4) + 16 * i, c8 = (tid & 15) * 8;
             const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&kv[i]);
             const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(&qv[i]);
             float kf[8], qf[8], kk = 0.f, qq = 0.f;
@@ -1155,15 +1162,12 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
             st4(sK + r * LD + c8 + 4, make_float4(kf[4], kf[5], kf[6], kf[7]));
             st4(sQ + r * LD + c8, make_float4(qf[0], qf[1], qf[2], qf[3]));
             st4(sQ + r * LD + c8 + 4, make_float4(qf[4], qf[5], qf[6], qf[7]));
-            *reinterpret_cast<uint4*>(sV + r * D + c8) = vv[i];
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int e = tid + i * THREADS, r = e >> 5, c4 = (e & 31) * 4;
+        for (int i = 0; i < 8; ++i) {
+            const int r = (tid >> 5) + 8 * i;
             float4 al = make_float4(1.f, 1.f, 1.f, 1.f);
             if (r < L) {
-                float4 db = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (a.dt_bias) db = *reinterpret_cast<const float4*>(a.dt_bias + (size_t)h * D + c4);
                 al.x = alpha_mufu(gv[i].x + db.x, rate, a.gp);
                 al.y = alpha_mufu(gv[i].y + db.y, rate, a.gp);
                 al.z = alpha_mufu(gv[i].z + db.z, rate, a.gp);
@@ -1173,198 +1177,242 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
         }
         if (tid < C) sBeta[tid] = tid < L ? sigmoid_f32(bt) : 0.f;
     }
-    for (int e = tid; e < C * LDA; e += THREADS) { sA[e] = 0.f; sP[e] = 0.f; }
+    tc::tc_fence_before();
     __syncthreads();
-
-    // 2. diagonal sub-blocks: thread (row j, column group cg), columns 4 cg + 32 m.  A warp holds
-    //    rows j = 4w .. 4w + 3, so rows r below the warp's first j are skipped uniformly.  The
-    //    per-thread partial sums of all 16 rows are reduced over the 8 column-group lanes at the
-    //    end with one transposed reduction (each lane ends with 4 of the 32 sums).
-    {
-        const int j = tid >> 3, cg = tid & 7, blk0 = j & ~15;
-        const int rstart = (j & 15) & ~3;
-        float4 kd[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) kd[m] = ld4(sK + j * LD + 4 * cg + 32 * m);
-        float red[32];                                // [0..15]: A partials, [16..31]: P partials
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-            red[rr] = 0.f;
-            red[16 + rr] = 0.f;
-            if (rr < rstart) continue;
-            const int r = blk0 + rr;
-            float pa[4], pp[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int c = 4 * cg + 32 * m;
-                if (r > j) kd[m] = mul4(kd[m], ld4(sAl + r * LD + c));
-                pa[m] = dot4(ld4(sK + r * LD + c), kd[m], 0.f);
-                pp[m] = dot4(ld4(sQ + r * LD + c), kd[m], 0.f);
-            }
-            red[rr] = (pa[0] + pa[1]) + (pa[2] + pa[3]);
-            red[16 + rr] = (pp[0] + pp[1]) + (pp[2] + pp[3]);
-        }
-        // transposed reduction over the 8 lanes of a row j: 16 + 8 + 4 shuffles
-#pragma unroll
-        for (int lvl = 0; lvl < 3; ++lvl) {
-            const int half = 16 >> lvl, off = 4 >> lvl;
-            const bool upper = (cg & off) != 0;
-#pragma unroll
-            for (int i = 0; i < half; ++i) {
-                const float keep = upper ? red[half + i] : red[i];
-                const float give = upper ? red[i] : red[half + i];
-                red[i] = keep + __shfl_xor_sync(0xffffffffu, give, off);
-            }
-        }
-        // lane cg now holds the totals of sums 4 cg .. 4 cg + 3
-        const int g = ((cg & 4) ? 4 : 0) + ((cg & 2) ? 2 : 0) + ((cg & 1) ? 1 : 0);
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const int idx = 4 * g + t;                // 0..31
-            const int rr = idx & 15;
-            const int r = blk0 + rr;
-            if (r >= j) {
-                if (idx < 16) {
-                    if (r > j) sA[r * LDA + j] = sBeta[r] * red[t];
-                } else {
-                    sP[r * LDA + j] = red[t];
-                }
-            }
-        }
-    }
-    __syncthreads();
-
-    // 3. per (column, sub-block): k o Rout -> sAl, k o Rin -> sK, q o Rin -> sQ, block product
-    {
-        const int c = tid & (D - 1), blk = tid >> 7;
-        float al[16], kk[16], qq[16];
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-            const int r = blk * 16 + rr;
-            al[rr] = sAl[r * LD + c];
-            kk[rr] = sK[r * LD + c];
-            qq[rr] = sQ[r * LD + c];
-        }
-        float rout = 1.f;
-#pragma unroll
-        for (int rr = 15; rr >= 0; --rr) {
-            sAl[(blk * 16 + rr) * LD + c] = kk[rr] * rout;
-            rout *= al[rr];
-        }
-        sBp[blk * D + c] = rout;
-        float rin = 1.f;
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-            rin *= al[rr];
-            sK[(blk * 16 + rr) * LD + c] = kk[rr] * rin;
-            sQ[(blk * 16 + rr) * LD + c] = qq[rr] * rin;
-        }
-    }
-    __syncthreads();
-
+    tc::tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    if (tid < D) {                                  // e^{G} at the block starts / after the block ends
-        const float b0 = sBp[tid], b1 = sBp[D + tid], b2 = sBp[2 * D + tid], b3 = sBp[3 * D + tid];
-        sEb[tid] = 1.f; sEb[D + tid] = b0; sEb[2 * D + tid] = b0 * b1; sEb[3 * D + tid] = (b0 * b1) * b2;
-        sEa[3 * D + tid] = 1.f; sEa[2 * D + tid] = b3; sEa[D + tid] = b3 * b2; sEa[tid] = (b3 * b2) * b1;
-    }
 
-    // 4a. Gram operands: B image rows n = 32 (I - 1) + {0..15: k o Rin, 16..31: q o Rin} of row block I;
-    //     TMEM lane m <- key j decayed to the start of block I: (k o Rout)[j] * prod_{J < bb < I} bp[bb]
-    for (int f = tid; f < 96 * D / 4; f += THREADS) {
-        const int core = f >> 3, n = (core >> 5) * 8 + (f & 7), c = (core & 31) * 4;
-        const int I = (n >> 5) + 1, w = n & 31;
-        const int r = 16 * I + (w & 15);
-        st4(sB + 4 * f, rnd4(ld4((w < 16 ? sK : sQ) + r * LD + c)));
+    // 2. diagonal sub-blocks.  Warp w: block w >> 1; lane = (jq, cg), 8 channel groups of 16
+    //    columns (4 cg + 32 m); the thread runs key row j = 4 (w & 1) + jq, then 15 - that, from the
+    //    first row its warp needs (rows below a thread's own j are computed and dropped).  The 32
+    //    partial sums of a row j (16 of A, 16 of P) are reduced over the 8 cg lanes at the end with
+    //    one transposed reduction (each lane ends with 4 of the totals).
+    {
+        const int blk = warp >> 1, cg = lane & 7, jq = lane >> 3;
+        const int blk0 = 16 * blk;
+#pragma unroll 1
+        for (int ps = 0; ps < 2; ++ps) {
+            const int jp = 4 * (warp & 1) + jq;
+            const int j = blk0 + (ps == 0 ? jp : 15 - jp);
+            const int rs = ps == 0 ? 4 * (warp & 1) : 12 - 4 * (warp & 1);   // warp-uniform
+            float4 kd[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) kd[m] = ld4(sK + j * LD + 4 * cg + 32 * m);
+            float red[32];
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+                red[rr] = 0.f;
+                red[16 + rr] = 0.f;
+                if (rr < rs) continue;
+                const int r = blk0 + rr;
+                float pa[4], pp[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int c = 4 * cg + 32 * m;
+                    if (r > j) kd[m] = mul4(kd[m], ld4(sAl + r * LD + c));
+                    pa[m] = dot4(ld4(sK + r * LD + c), kd[m], 0.f);
+                    pp[m] = dot4(ld4(sQ + r * LD + c), kd[m], 0.f);
+                }
+                red[rr] = (pa[0] + pa[1]) + (pa[2] + pa[3]);
+                red[16 + rr] = (pp[0] + pp[1]) + (pp[2] + pp[3]);
+            }
+#pragma unroll
+            for (int lvl = 0; lvl < 3; ++lvl) {
+                const int half = 16 >> lvl, off = 4 >> lvl;
+                const bool upper = (cg & off) != 0;
+#pragma unroll
+                for (int i = 0; i < half; ++i) {
+                    const float keep = upper ? red[half + i] : red[i];
+                    const float give = upper ? red[i] : red[half + i];
+                    red[i] = keep + __shfl_xor_sync(0xffffffffu, give, off);
+                }
+            }
+            // lane cg holds the totals of sums 4 cg .. 4 cg + 3 (0..15: A rows, 16..31: P rows)
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int idx = 4 * cg + t, rr = idx & 15, r = blk0 + rr;
+                if (idx < 16) sAD[r * 16 + (j & 15)] = r > j ? sBeta[r] * red[t] : 0.f;
+                else KDA_REC(P)[tc::img_index(r, j, C)] = r >= j ? tc::round_tf32(red[t]) : 0.f;
+            }
+        }
+        // zero upper off-diagonal blocks of the P image: (I, J) = (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+        for (int e = tid; e < 6 * 64; e += THREADS) {
+            const int b = e >> 6, i = (e >> 2) & 15, q4 = e & 3;
+            const int I = b < 3 ? 0 : (b < 5 ? 1 : 2);
+            const int J = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
+            st4(KDA_REC(P) + tc::img_index(16 * I + i, 16 * J + 4 * q4, C), make_float4(0.f, 0.f, 0.f, 0.f));
+        }
     }
-    if ((warp & 3) < 3) {          // lanes 0..95; warp quarter (warp >> 2) writes columns 32 q .. 32 q + 31
+    __syncthreads();
+
+    // 3. per (column c, sub-block): block products (every thread forms all four, in one order),
+    //    k o Rout -> alpha tile and Ktil^T record, k o Rin and q o Rin in place, (beta Kbar)^T -> TMEM
+    {
+        const int c = tid & (D - 1), hf = tid >> 7;
+        float bp[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            float p = 1.f;
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) p *= sAl[(16 * b + rr) * LD + c];
+            bp[b] = p;
+        }
+        sBp[(2 * hf) * D + c] = hf ? bp[2] : bp[0];
+        sBp[(2 * hf + 1) * D + c] = hf ? bp[3] : bp[1];
+        if (hf == 0) KDA_REC(GL)[c] = ((bp[0] * bp[1]) * bp[2]) * bp[3];
+#pragma unroll
+        for (int bi = 0; bi < 2; ++bi) {
+            const int blk = 2 * hf + bi;
+            float eb = 1.f, ea = 1.f;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                if (b < blk) eb *= bp[b];
+                if (b > blk) ea *= bp[b];
+            }
+            float al[16], kk[16], qq[16];
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+                const int r = 16 * blk + rr;
+                al[rr] = sAl[r * LD + c];
+                kk[rr] = sK[r * LD + c];
+                qq[rr] = sQ[r * LD + c];
+            }
+            float kt[16];
+            float rout = 1.f;
+#pragma unroll
+            for (int rr = 15; rr >= 0; --rr) {
+                const float ko = kk[rr] * rout;
+                sAl[(16 * blk + rr) * LD + c] = ko;
+                kt[rr] = tc::round_tf32(ko * ea);
+                rout *= al[rr];
+            }
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+                st4(KDA_REC(KT) + tc::img_index(c, 16 * blk + 4 * q4, C),
+                    make_float4(kt[4 * q4], kt[4 * q4 + 1], kt[4 * q4 + 2], kt[4 * q4 + 3]));
+            float kb[16];
+            float rin = 1.f;
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+                const int r = 16 * blk + rr;
+                rin *= al[rr];
+                const float ki = kk[rr] * rin;
+                sK[r * LD + c] = ki;
+                sQ[r * LD + c] = qq[rr] * rin;
+                kb[rr] = tc::round_tf32(sBeta[r] * ki * eb);
+            }
+            tc::tmem_st16_nowait(tmem + lane_base + T_KB + 16 * blk, kb);
+        }
+        tc::tmem_wait_st();
+    }
+    __syncthreads();
+
+    // 4. Gram operands and the Qbar record.  B image chunk f (16 bytes = 8 fp16 of one row) sits at
+    //    byte 16 f: core (n >> 3, c >> 3) = f >> 3, row n & 7 = f & 7; rows n = 32 (I - 1) + {0..15:
+    //    k o Rin, 16..31: q o Rin} of row block I.  Read now, written over the q tile after a barrier.
+    uint32_t bimg[6][4];
+#pragma unroll
+    for (int i = 0; i < 6; ++i) {
+        const int f = tid + THREADS * i, core = f >> 3;
+        const int n = (core >> 4) * 8 + (f & 7), c = (core & 15) * 8;
+        const int I = (n >> 5) + 1, w = n & 31;
+        const float* src = (w < 16 ? sK : sQ) + (16 * I + (w & 15)) * LD + c;
+        const float4 x0 = ld4(src), x1 = ld4(src + 4);
+        bimg[i][0] = tc::pack_f16x2(x0.x, x0.y);
+        bimg[i][1] = tc::pack_f16x2(x0.z, x0.w);
+        bimg[i][2] = tc::pack_f16x2(x1.x, x1.y);
+        bimg[i][3] = tc::pack_f16x2(x1.z, x1.w);
+    }
+    for (int f = tid; f < C * D / 4; f += THREADS) {          // Qbar: rows r, K = c
+        const int core = f >> 3, rr = (core >> 5) * 8 + (f & 7), c = (core & 31) * 4;
+        float4 eb = make_float4(1.f, 1.f, 1.f, 1.f);
+        for (int b = 0; b < (rr >> 4); ++b) eb = mul4(eb, ld4(sBp + b * D + c));
+        st4(KDA_REC(QB) + 4 * f, rnd4(mul4(ld4(sQ + rr * LD + c), eb)));
+    }
+    if ((warp & 3) < 3) {          // lanes 0..95: key j decayed to the start of row block I, fp16 pairs
         const int m = (warp & 3) * 32 + lane;
         int I, j;
         gram_row(m, I, j);
         const int J = j >> 4;
+        const int c0 = (warp >> 2) * 64;
+        uint32_t w32[32];
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-            const int c0 = (warp >> 2) * 32 + 16 * h2;
-            float x[16];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float4 v = ld4(sAl + j * LD + c0 + 4 * q4);
-                for (int bb = J + 1; bb < I; ++bb) v = mul4(v, ld4(sBp + bb * D + c0 + 4 * q4));
-                v = rnd4(v);
-                x[4 * q4] = v.x; x[4 * q4 + 1] = v.y; x[4 * q4 + 2] = v.z; x[4 * q4 + 3] = v.w;
-            }
-            tc::tmem_st16_nowait(tmem + lane_base + T_KD + c0, x);
+        for (int q4 = 0; q4 < 16; ++q4) {
+            const int c = c0 + 4 * q4;
+            float4 v = ld4(sAl + j * LD + c);
+            for (int bb = J + 1; bb < I; ++bb) v = mul4(v, ld4(sBp + bb * D + c));
+            w32[2 * q4] = tc::pack_f16x2(v.x, v.y);
+            w32[2 * q4 + 1] = tc::pack_f16x2(v.z, v.w);
         }
+        tc::tmem_st16u_nowait(tmem + lane_base + T_KD + c0 / 2, w32);
+        tc::tmem_st16u_nowait(tmem + lane_base + T_KD + c0 / 2 + 16, w32 + 16);
         tc::tmem_wait_st();
+    }
+    __syncthreads();               // k and q tiles are read; the alpha tile (k o Rout) is read
+#pragma unroll
+    for (int i = 0; i < 6; ++i)
+        *reinterpret_cast<uint4*>(sIB + 16 * (tid + THREADS * i)) = make_uint4(bimg[i][0], bimg[i][1], bimg[i][2], bimg[i][3]);
+    for (int e = tid; e < C * LDA; e += THREADS) {            // A <- diagonal blocks; T <- 0
+        const int r = e / LDA, jj = e - r * LDA;
+        sA[e] = (jj < C && (r >> 4) == (jj >> 4)) ? sAD[r * 16 + (jj & 15)] : 0.f;
+        sT[e] = 0.f;
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc::tc_fence_before();
     __syncthreads();
     if (tid == 0) {
         tc::tc_fence_after();
-        const uint32_t bB = tc::smem_u32(sB);
-        constexpr uint32_t idesc = tc::idesc_tf32(128, 96);
+        const uint32_t bB = tc::smem_u32(sIB);
+        constexpr uint32_t idesc = tc::idesc_f16(128, 96);
 #pragma unroll
-        for (int s = 0; s < D / 8; ++s)
-            tc::mma_tf32_ts(tmem + T_G, tmem + T_KD + 8 * s, tc::smem_desc(bB + 256 * s, 128, D * 32), idesc, s > 0);
+        for (int s = 0; s < D / 16; ++s)
+            tc::mma_f16_ts(tmem + T_G, tmem + T_KD + 8 * s, tc::smem_desc(bB + 256 * s, 128, 2048), idesc, s > 0);
         tc::mma_commit(bar_g);
     }
 
-    // 5. record: Qbar image, Ktil^T image, e^{G_L} (while the Gram MMA runs)
-    unsigned char* rec = reinterpret_cast<unsigned char*>(a.ws + ((size_t)ch * H + h) * a.ws_stride);
-    float* wW = reinterpret_cast<float*>(rec + TcRec::W);
-    float* wKT = reinterpret_cast<float*>(rec + TcRec::KT);
-    float* wU = reinterpret_cast<float*>(rec + TcRec::U);
-    float* wG = reinterpret_cast<float*>(rec + TcRec::GL);
-    float* wQ = reinterpret_cast<float*>(rec + TcRec::QB);
-    float* wP = reinterpret_cast<float*>(rec + TcRec::P);
-    for (int f = tid; f < C * D / 4; f += THREADS) {          // Qbar: rows r, K = c
-        const int core = f >> 3, rr = (core >> 5) * 8 + (f & 7), c = (core & 31) * 4;
-        st4(wQ + 4 * f, rnd4(mul4(ld4(sQ + rr * LD + c), ld4(sEb + (rr >> 4) * D + c))));
+    // 5. value loads for (beta V)^T (lane v, columns j = 32 jh ..), then the Gram result
+    const int vv_ = tid & (D - 1), jh = tid >> 7;
+    float vr[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int j = 32 * jh + i;
+        vr[i] = j < L ? __bfloat162float(vp[((size_t)(t0 + j) * H + h) * D + vv_]) : 0.f;
     }
-    for (int f = tid; f < C * D / 4; f += THREADS) {          // Ktil^T: rows c, K = r
-        const int core = f >> 3, cc = (core >> 4) * 8 + (f & 7), r0 = (core & 15) * 4;
-        const float ea = sEa[(r0 >> 4) * D + cc];
-        const float4 v = make_float4(sAl[r0 * LD + cc] * ea, sAl[(r0 + 1) * LD + cc] * ea,
-                                     sAl[(r0 + 2) * LD + cc] * ea, sAl[(r0 + 3) * LD + cc] * ea);
-        st4(wKT + 4 * f, rnd4(v));
-    }
-    if (tid < D) wG[tid] = sEb[3 * D + tid] * sBp[3 * D + tid];
-    // 4b. Gram result -> off-diagonal blocks of A and P
-    if (warp < 3) {
+    {
         const bool done = tc::mbar_wait(bar_g, 0, kWaitPolls);
         tc::tc_fence_after();
-        if (!done && lane == 0) record_error(kDevErrTimeout);
-        const int m = tid;
+        if (!done && tid == 0) record_error(kDevErrTimeout);
+    }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = tc::round_tf32(sBeta[32 * jh + 16 * hh + i] * vr[16 * hh + i]);
+        tc::tmem_st16_nowait(tmem + lane_base + T_KD + 32 * jh + 16 * hh, x);
+    }
+    if ((warp & 3) < 3) {          // Gram rows m = (I, j): warp half 0 -> A (k rows), half 1 -> P (q rows)
+        const int q = warp & 3, hf = warp >> 2;
+        const int m = 32 * q + lane;
         int I, j;
         gram_row(m, I, j);
-        float g[96];
-        tc::tmem_ld32(tmem + lane_base + T_G, g);
-        tc::tmem_ld32(tmem + lane_base + T_G + 32, g + 32);
-        tc::tmem_ld32(tmem + lane_base + T_G + 64, g + 64);
+        const int Ia = q + 1, Ib = q < 2 ? q + 2 : 3;
+        float ga[16], gb[16];
+        tc::tmem_ld16(tmem + lane_base + T_G + 32 * (Ia - 1) + 16 * hf, ga);
+        tc::tmem_ld16(tmem + lane_base + T_G + 32 * (Ib - 1) + 16 * hf, gb);
 #pragma unroll
-        for (int Ib = 1; Ib <= 3; ++Ib) {
-            if (Ib == I) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int r = 16 * I + i;
-                    sA[r * LDA + j] = sBeta[r] * g[32 * (Ib - 1) + i];
-                    sP[r * LDA + j] = g[32 * (Ib - 1) + 16 + i];
-                }
-            }
+        for (int i = 0; i < 16; ++i) {
+            const int r = 16 * I + i;
+            const float g = I == Ia ? ga[i] : gb[i];
+            if (hf == 0) sA[r * LDA + j] = sBeta[r] * g;
+            else KDA_REC(P)[tc::img_index(r, j, C)] = tc::round_tf32(g);
         }
     }
+    tc::tmem_wait_st();
     tc::tc_fence_before();
     __syncthreads();
 
-    // P image (rows r, K = j); T diagonal blocks (R1 is free: the Gram MMA has completed)
-    for (int f = tid; f < C * C / 4; f += THREADS) {
-        const int core = f >> 3, rr = (core >> 4) * 8 + (f & 7), j0 = (core & 15) * 4;
-        st4(wP + 4 * f, rnd4(ld4(sP + rr * LDA + j0)));
-    }
-    for (int e = tid; e < C * LDA; e += THREADS) sT[e] = 0.f;
-    __syncthreads();
+    // 6. T = (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution, then by block distance
     if (tid < C) {
         const int I = tid >> 4, jj = tid & 15, j = tid;
         float col[16];
@@ -1381,7 +1429,6 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
         for (int i = 0; i < 16; ++i) sT[(16 * I + i) * LDA + j] = col[i];
     }
     __syncthreads();
-    // 6. off-diagonal blocks of T, by block distance d (loops unrolled so the loads issue together)
     auto tblocks = [&](auto dc) {
         constexpr int d = decltype(dc)::value;
         constexpr int nb = NB - d;
@@ -1410,63 +1457,44 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
     tblocks(std::integral_constant<int, 2>{});
     tblocks(std::integral_constant<int, 3>{});
 
-    // 7. operand images: T (rows r, K = j), (beta V)^T (rows v, K = j), (beta Kbar)^T (rows c, K = j)
-    float* sIV = reinterpret_cast<float*>(sm + OFF_IV);
-    float* sIK = reinterpret_cast<float*>(sm + OFF_IK);
+    // T image (rows r, K = j); U^T = (beta V)^T T^T, W^T = (beta Kbar)^T T^T
     for (int f = tid; f < C * C / 4; f += THREADS) {
         const int core = f >> 3, rr = (core >> 4) * 8 + (f & 7), j0 = (core & 15) * 4;
         st4(sIT + 4 * f, rnd4(ld4(sT + rr * LDA + j0)));
     }
-    for (int f = tid; f < D * C / 4; f += THREADS) {
-        const int core = f >> 3, row = (core >> 4) * 8 + (f & 7), j0 = (core & 15) * 4;
-        float4 vv, kb;
-        float* pv = &vv.x;
-        float* pk = &kb.x;
-        const float eb = sEb[(j0 >> 4) * D + row];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int j = j0 + i;
-            pv[i] = sBeta[j] * __bfloat162float(sV[j * D + row]);
-            pk[i] = sBeta[j] * sK[j * LD + row] * eb;
-        }
-        st4(sIV + 4 * f, rnd4(vv));
-        st4(sIK + 4 * f, rnd4(kb));
-    }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc::tc_fence_before();
     __syncthreads();
-
-    // 8. U^T = (beta V)^T T^T, W^T = (beta Kbar)^T T^T
     if (tid == 0) {
         tc::tc_fence_after();
         constexpr uint32_t idesc = tc::idesc_tf32(128, 64);
-        const uint32_t aV = tc::smem_u32(sIV), aK = tc::smem_u32(sIK), bT = tc::smem_u32(sIT);
+        const uint32_t bT = tc::smem_u32(sIT);
 #pragma unroll
         for (int s = 0; s < C / 8; ++s)
-            tc::mma_tf32_ss(tmem + T_U, tc::smem_desc(aV + 256 * s, 128, 2048), tc::smem_desc(bT + 256 * s, 128, 2048), idesc, s > 0);
+            tc::mma_tf32_ts(tmem + T_G, tmem + T_KD + 8 * s, tc::smem_desc(bT + 256 * s, 128, 2048), idesc, s > 0);
 #pragma unroll
         for (int s = 0; s < C / 8; ++s)
-            tc::mma_tf32_ss(tmem + T_W, tc::smem_desc(aK + 256 * s, 128, 2048), tc::smem_desc(bT + 256 * s, 128, 2048), idesc, s > 0);
+            tc::mma_tf32_ts(tmem + T_G + 64, tmem + T_KB + 8 * s, tc::smem_desc(bT + 256 * s, 128, 2048), idesc, s > 0);
         tc::mma_commit(bar_uw);
     }
-    if (warp < 8) {
+    {
         const bool done = tc::mbar_wait(bar_uw, 0, kWaitPolls);
         tc::tc_fence_after();
         if (!done) {
             if (lane == 0) record_error(kDevErrTimeout);
         } else {
-            const int row = (warp & 3) * 32 + lane;
-            const uint32_t taddr = tmem + lane_base + (warp < 4 ? T_U : T_W);
+            const int row = (warp & 3) * 32 + lane, hf = warp >> 2;
+            const uint32_t taddr = tmem + lane_base + T_G + 64 * hf;
 #pragma unroll
             for (int r0 = 0; r0 < C; r0 += 16) {
                 float x[16];
                 tc::tmem_ld16(taddr + r0, x);
-                if (warp < 4) {
+                if (hf == 0) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) wU[(r0 + j) * D + row] = x[j];
+                    for (int j = 0; j < 16; ++j) KDA_REC(U)[(r0 + j) * D + row] = x[j];
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) wW[tc::img_index(r0 + j, row, D)] = tc::round_tf32(x[j]);
+                    for (int j = 0; j < 16; ++j) KDA_REC(W)[tc::img_index(r0 + j, row, D)] = tc::round_tf32(x[j]);
                 }
             }
         }
@@ -1475,8 +1503,9 @@ __global__ void __launch_bounds__(itc::THREADS, 1) chunk_intra_tc_kernel(const I
     __syncthreads();
     if (warp == 0) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem, 512);
+        tc::tmem_dealloc(tmem, 256);
     }
+#undef KDA_REC
 }
 
 // ---- host-side dispatch --------------------------------------------------------------------------
@@ -1517,6 +1546,9 @@ cudaError_t run_prefill(const kda_params& p, const GateParams& gp, const void* q
     dim3 gi((unsigned)w.max_chunks, (unsigned)H);
     if constexpr (kTensorCore) {
         e = cudaFuncSetAttribute(chunk_intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)itc::BYTES);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(chunk_intra_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         chunk_intra_tc_kernel<<<gi, itc::THREADS, itc::BYTES, stream>>>(ia);
     } else {

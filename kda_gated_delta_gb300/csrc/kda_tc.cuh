@@ -1,11 +1,14 @@
 // kda_tc.cuh -- thin inline-PTX wrappers for the Blackwell (sm_100a / sm_103a) tensor-core path:
 // mbarriers, bulk async copies (TMA engine, non-tensor form), tensor memory (TMEM) allocation,
-// tcgen05.mma of kind::tf32, tcgen05.commit, tcgen05.ld / tcgen05.st and the tcgen05 fences.
+// tcgen05.mma of kind::tf32 and kind::f16, tcgen05.commit, tcgen05.ld / tcgen05.st and the
+// tcgen05 fences.
 //
-// Operand images in shared memory use the canonical no-swizzle K-major layout: the tile of R rows
-// by K tf32 elements is cut into "core matrices" of 8 rows x 4 elements (16 bytes per row, 128
-// bytes per core matrix); core (row group rg, k group kc) sits at byte rg * SBO + kc * LBO with
-// LBO = 128 (k groups adjacent) and SBO = K * 32 (one 8-row slab holds all K).
+// Operand images in shared memory use the canonical no-swizzle K-major layout: the tile is cut
+// into "core matrices" of 8 rows x 16 bytes (4 tf32 or 8 fp16 elements per row, 128 bytes per
+// core matrix); core (row group rg, k group kc) sits at byte rg * SBO + kc * LBO with LBO = 128
+// (k groups adjacent) and SBO = 8 rows x the row's bytes (one 8-row slab holds all K).  One MMA
+// step consumes 32 bytes of K (8 tf32 or 16 fp16), i.e. two core matrices: the descriptor start
+// advances by 256 bytes per step.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -55,6 +58,23 @@ __host__ __device__ constexpr uint32_t idesc_tf32(uint32_t M, uint32_t N)
          | (2u << 10)           // B format: tf32
          | ((N >> 3) << 17)     // N / 8
          | ((M >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor of kind::f16 with fp16 A and B (both K-major) and an fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N)
+{
+    return (1u << 4)            // D format: f32
+         | ((N >> 3) << 17)     // N / 8   (A and B format 0 = f16)
+         | ((M >> 4) << 24);    // M / 16
+}
+
+// Two fp32 values rounded to fp16 (nearest even) and packed: lo in bits 0..15, hi in 16..31.
+// This is the order a kind::f16 A operand in TMEM expects: column c holds k = 2c and 2c + 1.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 // ---- mbarriers ----------------------------------------------------------------------------------
@@ -152,6 +172,18 @@ __device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc]^T    (kind::f16: fp16 A in TMEM as packed pairs, fp16 B image)
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive (once) on *bar when every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar)
 {
@@ -209,6 +241,15 @@ __device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const float* v)
         "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
         "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
         "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st16u_nowait(uint32_t taddr, const uint32_t* v)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
