@@ -1006,6 +1006,39 @@ __device__ __forceinline__ float alpha_mufu(float x, float rate, const GateParam
     const float sp2 = x > gp.softplus_threshold ? x * kLog2e : lg2_approx(1.0f + ex2_approx(x * kLog2e));
     return ex2_approx(-rate * sp2);
 }
+// Packed fp32 pairs (one 64-bit register pair) and the sm_100+ paired FP32 instructions; each lane
+// of a pair is an ordinary IEEE fp32 multiply / fused multiply-add.
+__device__ __forceinline__ uint64_t f2pack(float x, float y)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ float f2sum(uint64_t r)
+{
+    float x, y;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(r));
+    return x + y;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+// 16 bytes of shared memory as two packed pairs
+__device__ __forceinline__ void ld2x2(const float* p, uint64_t& lo, uint64_t& hi)
+{
+    const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(p);
+    lo = v.x;
+    hi = v.y;
+}
 // Gram row m (0..95) -> row block I and key row j
 __device__ __forceinline__ void gram_row(int m, int& I, int& j)
 {
@@ -1040,8 +1073,10 @@ constexpr uint32_t OFF_K = 0;                        // k_hat -> k o Rin; then A
 constexpr uint32_t OFF_Q = TILE;                     // q_hat -> q o Rin; then the Gram B image
 constexpr uint32_t OFF_AL = 2 * TILE;                // alpha -> k o Rout; then T and its image
 constexpr uint32_t OFF_AD = 3 * TILE;                // diagonal blocks of A   [NB][16][16]
-constexpr uint32_t OFF_BP = OFF_AD + NB * 256 * 4;   // block products         [NB][D]
-constexpr uint32_t OFF_BETA = OFF_BP + NB * D * 4;   // beta                   [C]
+constexpr uint32_t OFF_BP = OFF_AD + NB * 256 * 4;   // block products bp      [NB][D]
+constexpr uint32_t OFF_EB = OFF_BP + NB * D * 4;     // e^{G} before block b: prod_{b' < b} bp  [NB][D]
+constexpr uint32_t OFF_B12 = OFF_EB + NB * D * 4;    // bp[1] * bp[2]          [D]
+constexpr uint32_t OFF_BETA = OFF_B12 + D * 4;       // beta                   [C]
 constexpr uint32_t OFF_BAR = OFF_BETA + C * 4;       // 2 mbarriers
 constexpr uint32_t OFF_TM = OFF_BAR + 16;            // TMEM base
 constexpr uint32_t BYTES = OFF_TM + 16;
@@ -1070,6 +1105,8 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
     float* sAl = reinterpret_cast<float*>(sm + OFF_AL);
     float* sAD = reinterpret_cast<float*>(sm + OFF_AD);
     float* sBp = reinterpret_cast<float*>(sm + OFF_BP);
+    float* sEb = reinterpret_cast<float*>(sm + OFF_EB);
+    float* sB12 = reinterpret_cast<float*>(sm + OFF_B12);
     float* sBeta = reinterpret_cast<float*>(sm + OFF_BETA);
     float* sA = reinterpret_cast<float*>(sm + OFF_A);
     float* sX = reinterpret_cast<float*>(sm + OFF_X);
@@ -1109,6 +1146,11 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
         tc::mbar_init(bar_g, 1);
         tc::mbar_init(bar_uw, 1);
         tc::fence_mbar_init();
+    }
+    if (warp == 1) {               // the value rows are read after the Gram: start them towards L2 now
+        for (int r = lane; r < L; r += 32)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], 256;" ::"l"(vp + ((size_t)(t0 + r) * H + h) * D)
+                         : "memory");
     }
     // 1. loads, all issued before any is used (rows past the chunk end: k = q = 0, alpha = 1,
     //    beta = 0).  k, q: 8 elements in rows (tid >> 4) + 16 i; g: 4 elements in rows (tid >> 5) + 8 i
@@ -1196,9 +1238,9 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
             const int jp = 4 * (warp & 1) + jq;
             const int j = blk0 + (ps == 0 ? jp : 15 - jp);
             const int rs = ps == 0 ? 4 * (warp & 1) : 12 - 4 * (warp & 1);   // warp-uniform
-            float4 kd[4];
+            uint64_t kd[8];                       // key j decayed to row r, as packed pairs
 #pragma unroll
-            for (int m = 0; m < 4; ++m) kd[m] = ld4(sK + j * LD + 4 * cg + 32 * m);
+            for (int m = 0; m < 4; ++m) ld2x2(sK + j * LD + 4 * cg + 32 * m, kd[2 * m], kd[2 * m + 1]);
             float red[32];
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) {
@@ -1206,16 +1248,25 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
                 red[16 + rr] = 0.f;
                 if (rr < rs) continue;
                 const int r = blk0 + rr;
-                float pa[4], pp[4];
+                uint64_t pa0 = 0, pa1 = 0, pp0 = 0, pp1 = 0;
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const int c = 4 * cg + 32 * m;
-                    if (r > j) kd[m] = mul4(kd[m], ld4(sAl + r * LD + c));
-                    pa[m] = dot4(ld4(sK + r * LD + c), kd[m], 0.f);
-                    pp[m] = dot4(ld4(sQ + r * LD + c), kd[m], 0.f);
+                    uint64_t x0, x1;
+                    if (r > j) {
+                        ld2x2(sAl + r * LD + c, x0, x1);
+                        kd[2 * m] = mul2(kd[2 * m], x0);
+                        kd[2 * m + 1] = mul2(kd[2 * m + 1], x1);
+                    }
+                    ld2x2(sK + r * LD + c, x0, x1);
+                    pa0 = fma2(x0, kd[2 * m], pa0);
+                    pa1 = fma2(x1, kd[2 * m + 1], pa1);
+                    ld2x2(sQ + r * LD + c, x0, x1);
+                    pp0 = fma2(x0, kd[2 * m], pp0);
+                    pp1 = fma2(x1, kd[2 * m + 1], pp1);
                 }
-                red[rr] = (pa[0] + pa[1]) + (pa[2] + pa[3]);
-                red[16 + rr] = (pp[0] + pp[1]) + (pp[2] + pp[3]);
+                red[rr] = f2sum(pa0) + f2sum(pa1);
+                red[16 + rr] = f2sum(pp0) + f2sum(pp1);
             }
 #pragma unroll
             for (int lvl = 0; lvl < 3; ++lvl) {
@@ -1260,7 +1311,10 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
         }
         sBp[(2 * hf) * D + c] = hf ? bp[2] : bp[0];
         sBp[(2 * hf + 1) * D + c] = hf ? bp[3] : bp[1];
-        if (hf == 0) KDA_REC(GL)[c] = ((bp[0] * bp[1]) * bp[2]) * bp[3];
+        if (hf == 0) {
+            KDA_REC(GL)[c] = ((bp[0] * bp[1]) * bp[2]) * bp[3];
+            sB12[c] = bp[1] * bp[2];
+        }
 #pragma unroll
         for (int bi = 0; bi < 2; ++bi) {
             const int blk = 2 * hf + bi;
@@ -1270,6 +1324,7 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
                 if (b < blk) eb *= bp[b];
                 if (b > blk) ea *= bp[b];
             }
+            sEb[blk * D + c] = eb;
             float al[16], kk[16], qq[16];
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) {
@@ -1326,9 +1381,7 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
     }
     for (int f = tid; f < C * D / 4; f += THREADS) {          // Qbar: rows r, K = c
         const int core = f >> 3, rr = (core >> 5) * 8 + (f & 7), c = (core & 31) * 4;
-        float4 eb = make_float4(1.f, 1.f, 1.f, 1.f);
-        for (int b = 0; b < (rr >> 4); ++b) eb = mul4(eb, ld4(sBp + b * D + c));
-        st4(KDA_REC(QB) + 4 * f, rnd4(mul4(ld4(sQ + rr * LD + c), eb)));
+        st4(KDA_REC(QB) + 4 * f, rnd4(mul4(ld4(sQ + rr * LD + c), ld4(sEb + (rr >> 4) * D + c))));
     }
     if ((warp & 3) < 3) {          // lanes 0..95: key j decayed to the start of row block I, fp16 pairs
         const int m = (warp & 3) * 32 + lane;
@@ -1336,12 +1389,14 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
         gram_row(m, I, j);
         const int J = j >> 4;
         const int c0 = (warp >> 2) * 64;
+        // decay over the whole blocks between J and I: none, bp[1], bp[2] or bp[1] bp[2]
+        const float* mid = I - J < 2 ? nullptr : (I - J == 3 ? sB12 : sBp + (J + 1) * D);
         uint32_t w32[32];
 #pragma unroll
         for (int q4 = 0; q4 < 16; ++q4) {
             const int c = c0 + 4 * q4;
             float4 v = ld4(sAl + j * LD + c);
-            for (int bb = J + 1; bb < I; ++bb) v = mul4(v, ld4(sBp + bb * D + c));
+            if (mid) v = mul4(v, ld4(mid + c));
             w32[2 * q4] = tc::pack_f16x2(v.x, v.y);
             w32[2 * q4 + 1] = tc::pack_f16x2(v.z, v.w);
         }
