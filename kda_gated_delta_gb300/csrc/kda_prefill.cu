@@ -681,21 +681,24 @@ __global__ void __launch_bounds__(256, 1) chunk_state_kernel(const StateArgs a)
 }
 
 // ---- inter-chunk state pass on the tensor cores (C = 64, D = 128) --------------------------------
-// One CTA of 256 threads per (sequence, head).  Warps 0..3 run the serial chain: thread v owns
-// value row v, whose row of S^T lives in registers (fp32), and it is TMEM lane v.  Per chunk, in the
-// transposed ("value-major") form so that every MMA has M = 128 rows = the 128 value rows:
+// One CTA of 256 threads per (sequence, head), in the transposed ("value-major") form so that every
+// MMA has M = 128 rows = the 128 value rows (TMEM lane v).  Per chunk:
 //   (a)  Dd   = S^T W^T                  A = tf32 copy of S^T in TMEM, B = W image       (N = 64)
-//   threads: Delta^T = U^T - Dd -> tf32 copy in TMEM
-//   (b2) Do   = Delta^T P^T              A = Delta^T in TMEM,          B = P image       (N = 64)
-//   (c)  Dc   = Delta^T Ktil             A = Delta^T,                  B = Ktil^T image  (N = 128)
-//   (b)  Do  += S^T Qbar^T               A = S^T,                      B = Qbar image    (N = 64)
-//   threads: S^T <- S^T Diag(e^{G_L}) + Dc (fp32), refresh the tf32 copy
-// Warps 4..7 (the same TMEM lane quarters) copy O^T = Do of each chunk to the output while the
-// chain goes on: Do alternates between two TMEM buffers, the chain signals a filled buffer with a
-// commit and the output warps hand it back with 128 arrivals, so no output write sits on the chain.
-// Operand images arrive by bulk async copy from the record: W and U/gL are double-buffered
-// (loaded two chunks ahead); Qbar, P and Ktil^T are reloaded as soon as the chunk's MMAs retire.
-// All waits are bounded.
+//   chain threads: Delta^T = U^T - Dd, rounded to tf32, written over Dd
+//   (c)  Dc   = Delta^T Ktil             A = Delta^T in TMEM,          B = Ktil^T image  (N = 128)
+//   chain threads: S^T <- S^T Diag(e^{G_L}) + Dc (fp32 in registers), tf32 copy to the other buffer
+//   (b2) Do   = Delta^T P^T              A = Delta^T,                  B = P image       (N = 64)
+//   (b)  Do  += S^T Qbar^T               A = S^T (this chunk's copy),  B = Qbar image    (N = 64)
+//   output threads: O^T = Do -> out
+// Warps 0..3 run the serial chain ((a), Delta, (c), S update): thread v owns value row v of S^T in
+// registers.  Warps 4..7 produce the output: thread 128 issues (b2) and (b) once Delta is ready and
+// P / Qbar have landed, and the four warps copy Do to the output, so neither the output MMAs nor
+// their operands (P, Qbar) sit on the chain.  The S^T copy is double-buffered (chunk i reads buffer
+// i & 1), so the S update of chunk i only waits for (b) of chunk i - 1.  Hand-offs: mbarriers
+// (delta_ready: chain -> issuer; b2_done, out_ready[2]: tensor-core commits of the issuer).
+// Operand images arrive by bulk async copy from the record: W and U/gL double-buffered (two chunks
+// ahead), Ktil^T, P and Qbar one chunk ahead.  All waits are bounded and give up early once either
+// side has recorded a failure.
 constexpr uint32_t kWaitPolls = 1u << 24;
 
 // shared memory: the record image (one buffer set) followed by the second W and U/gL buffers
@@ -705,24 +708,25 @@ constexpr uint32_t kUGBytes = 32768 + 512;
 constexpr uint32_t kSmBars = kSmUG1 + kUGBytes;
 struct TcBars {
     uint64_t w[2], ug[2], kt, qb, p;  // operand buffers filled (tx bytes); these seven come first
-    uint64_t mma_a;                   // (a) complete
-    uint64_t mma_c;                   // (a), (b2), (c), (b) complete
-    uint64_t out_ready[2];            // O^T of chunk i is in TMEM buffer i & 1 (same point as mma_c)
-    uint64_t out_free[2];             // the output warps have read buffer i & 1 (128 arrivals)
-    uint64_t drain;                   // used once, to drain the tensor core after a failed wait
+    uint64_t mma_a;                   // (a) complete                    (chain commit)
+    uint64_t mma_c;                   // (c) complete                    (chain commit)
+    uint64_t delta_ready;             // Delta^T of the chunk is in TMEM (chain thread 0 arrives)
+    uint64_t b2_done;                 // (b2) complete: Delta^T may be overwritten (issuer commit)
+    uint64_t out_ready[2];            // (b) of chunk i complete, Do ready; index i & 1 (issuer commit)
+    uint64_t drain[2];                // used once each, to drain the tensor core after a failed wait
 };
 constexpr size_t kTcSmemBytes = kSmBars + 1024;
 static_assert(sizeof(TcBars) + 32 + 512 <= 1024, "barriers, TMEM base, abort flag and e^{G_L}");
 static_assert(kTcSmemBytes <= 232448, "state-pass shared memory");
 
 // TMEM column map (512 columns allocated; each accumulator starts at a multiple of its width)
-constexpr uint32_t kT_SOP = 0;     // tf32 S^T        (128 cols, A operand)
-constexpr uint32_t kT_SC = 128;    // Delta^T Ktil    (128, accumulator)
-constexpr uint32_t kT_DD = 256;    // S^T W^T         (64, accumulator)
-constexpr uint32_t kT_DOP = 320;   // tf32 Delta^T    (64, A operand)
-constexpr uint32_t kT_OUT = 384;   // O^T, two buffers (2 x 64, accumulators)
+constexpr uint32_t kT_SOP = 0;     // tf32 S^T, two buffers   (2 x 128 cols, A operand)
+constexpr uint32_t kT_SC = 256;    // Delta^T Ktil            (128, accumulator)
+constexpr uint32_t kT_DD = 384;    // S^T W^T, then Delta^T   (64, accumulator, then A operand)
+constexpr uint32_t kT_OUT = 448;   // O^T                     (64, accumulator)
 
 __device__ __forceinline__ void chain_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void output_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 template <typename TOut>
 __global__ void __launch_bounds__(256, 1) chunk_state_tc_kernel(const StateArgs a)
@@ -733,6 +737,7 @@ __global__ void __launch_bounds__(256, 1) chunk_state_tc_kernel(const StateArgs 
     TcBars* bars = reinterpret_cast<TcBars*>(sm + kSmBars);
     uint32_t* s_taddr = reinterpret_cast<uint32_t*>(sm + kSmBars + sizeof(TcBars));
     volatile int* s_abort = reinterpret_cast<volatile int*>(sm + kSmBars + sizeof(TcBars) + 16);
+    float* s_gl = reinterpret_cast<float*>(sm + kSmBars + sizeof(TcBars) + 32);  // e^{G_L} of the chunk
 
     // longest sequences first: CTA x -> (rank, head), rank -> sequence through seq_order
     const int H = a.H;
@@ -766,8 +771,6 @@ __global__ void __launch_bounds__(256, 1) chunk_state_tc_kernel(const StateArgs 
     if (tid == 0) {
         uint64_t* b = reinterpret_cast<uint64_t*>(bars);
         for (int i = 0; i < (int)(sizeof(TcBars) / 8); ++i) tc::mbar_init(b + i, 1);
-        tc::mbar_init(&bars->out_free[0], 128);
-        tc::mbar_init(&bars->out_free[1], 128);
         *s_abort = 0;
         tc::fence_mbar_init();
     }
@@ -777,69 +780,106 @@ __global__ void __launch_bounds__(256, 1) chunk_state_tc_kernel(const StateArgs 
     const uint32_t tmem = *s_taddr;
     const uint32_t lane = (uint32_t)((warp & 3) * 32) << 16;
 
+    // bounded wait that also gives up once the other side has recorded a failure
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        for (uint32_t it = 0; it < kWaitPolls; ++it) {
+            if (tc::mbar_try_wait(bar, parity)) return true;
+            if ((it & 63u) == 63u && *s_abort) return false;
+        }
+        *s_abort = 1;
+        return false;
+    };
+    auto rec_of = [&](int64_t ch) -> const unsigned char* {
+        return reinterpret_cast<const unsigned char*>(a.ws + ((size_t)ch * H + h) * a.ws_stride);
+    };
+    // copies in flight per load barrier (bookkeeping of the issuing thread, for the drain)
+    uint64_t* const bar0 = &bars->w[0];
+    uint32_t pend_mask = 0, pend_par = 0, uses[7] = {0, 0, 0, 0, 0, 0, 0};
+    auto load = [&](uint64_t* bar, uint32_t dst_off, uint32_t src_off, uint32_t bytes, int64_t ch) {
+        const uint32_t bi = (uint32_t)(bar - bar0), bit = 1u << bi;
+        pend_mask |= bit;
+        pend_par = (pend_par & ~bit) | ((uses[bi] & 1u) ? bit : 0u);
+        ++uses[bi];
+        tc::mbar_arrive_expect_tx(bar, bytes);
+        tc::bulk_g2s(sm + dst_off, rec_of(ch) + src_off, bytes, bar);
+    };
+    auto landed = [&](uint64_t* bar) { pend_mask &= ~(1u << (uint32_t)(bar - bar0)); };
+    auto drain = [&](uint64_t* dbar) {          // after a failure: own MMAs and copies land, bounded
+        tc::mma_commit(dbar);
+        tc::mbar_wait(dbar, 0, kWaitPolls);
+        for (uint32_t bi = 0; bi < 7; ++bi)
+            if (pend_mask & (1u << bi)) tc::mbar_wait(bar0 + bi, (pend_par >> bi) & 1u, kWaitPolls);
+    };
+    constexpr uint32_t kId64 = tc::idesc_tf32(128, 64), kId128 = tc::idesc_tf32(128, 128);
+
     if (warp >= 4) {
-        // ---- output warps: O^T of chunk i (TMEM buffer i & 1) -> out, then hand the buffer back
+        // ---- output side: thread 128 issues (b2) and (b); warps 4..7 copy Do to the output
         const int v = tid - 128;
-        for (int64_t ch = c_begin; ch < c_end; ++ch) {
-            const uint32_t i = (uint32_t)(ch - c_begin), ob = i & 1u;
-            bool ready = false;
-            for (uint32_t it = 0; it < kWaitPolls && !ready; ++it) {
-                ready = tc::mbar_try_wait(&bars->out_ready[ob], (i >> 1) & 1u);
-                if (!ready && *s_abort) break;
-            }
-            if (!ready) {
-                if (!*s_abort) {                         // the chain is stuck without saying so
-                    *s_abort = 1;
-                    if (v == 0) record_error(kDevErrTimeout);
+        const bool issuer = (v == 0);
+        const uint32_t sQB = tc::smem_u32(sm + TcRec::QB), sP = tc::smem_u32(sm + TcRec::P);
+        if (issuer) {
+            load(&bars->p, TcRec::P, TcRec::P, 16384, c_begin);
+            load(&bars->qb, TcRec::QB, TcRec::QB, 32768, c_begin);
+        }
+        bool ok = true;
+        for (int64_t ch = c_begin; ch < c_end && ok; ++ch) {
+            const uint32_t i = (uint32_t)(ch - c_begin), ph = i & 1u;
+            if (issuer) {
+                ok = wait(&bars->delta_ready, ph) && wait(&bars->p, ph);
+                if (ok) {
+                    landed(&bars->p);
+                    tc::tc_fence_after();
+#pragma unroll
+                    for (int s = 0; s < C / 8; ++s)
+                        tc::mma_tf32_ts(tmem + kT_OUT, tmem + kT_DD + 8 * s, tc::smem_desc(sP + 256 * s, 128, 2048), kId64, s > 0);
+                    tc::mma_commit(&bars->b2_done);
+                    ok = wait(&bars->qb, ph);
                 }
-                break;
+                if (ok) {
+                    landed(&bars->qb);
+#pragma unroll
+                    for (int s = 0; s < D / 8; ++s)
+                        tc::mma_tf32_ts(tmem + kT_OUT, tmem + kT_SOP + 128 * (i & 1u) + 8 * s,
+                                        tc::smem_desc(sQB + 256 * s, 128, 4096), kId64, 1);
+                    tc::mma_commit(&bars->out_ready[i & 1u]);
+                }
             }
+            ok = wait(&bars->out_ready[i & 1u], (i >> 1) & 1u);   // every output thread
+            if (!ok) break;
             tc::tc_fence_after();
+            if (issuer && ch + 1 < c_end) {            // (b2) and (b) are done with P and Qbar
+                load(&bars->p, TcRec::P, TcRec::P, 16384, ch + 1);
+                load(&bars->qb, TcRec::QB, TcRec::QB, 32768, ch + 1);
+            }
             const int64_t t0 = a.chunk_start[ch];
             const int L = a.chunk_len[ch];
 #pragma unroll
             for (int r0 = 0; r0 < C; r0 += 16) {
                 float o[16];
-                tc::tmem_ld16(tmem + lane + kT_OUT + 64 * ob + r0, o);
+                tc::tmem_ld16(tmem + lane + kT_OUT + r0, o);
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     if (r0 + j < L) out[((size_t)(t0 + r0 + j) * H + h) * D + v] = from_f32<TOut>(o[j]);
             }
             tc::tc_fence_before();
-            tc::mbar_arrive(&bars->out_free[ob]);
+            output_sync();                             // Do is free for the next chunk's (b2)
         }
+        if (issuer && *s_abort) drain(&bars->drain[1]);
     } else {
         // ---- the chain (warps 0..3)
-        auto rec_of = [&](int64_t ch) -> const unsigned char* {
-            return reinterpret_cast<const unsigned char*>(a.ws + ((size_t)ch * H + h) * a.ws_stride);
-        };
-        // copies in flight per load barrier (thread 0's bookkeeping, for the drain after a failed wait)
-        uint64_t* const bar0 = &bars->w[0];
-        uint32_t pend_mask = 0, pend_par = 0, uses[7] = {0, 0, 0, 0, 0, 0, 0};
-        auto load = [&](uint64_t* bar, uint32_t dst_off, uint32_t src_off, uint32_t bytes, int64_t ch) {
-            const uint32_t bi = (uint32_t)(bar - bar0), bit = 1u << bi;
-            pend_mask |= bit;
-            pend_par = (pend_par & ~bit) | ((uses[bi] & 1u) ? bit : 0u);
-            ++uses[bi];
-            tc::mbar_arrive_expect_tx(bar, bytes);
-            tc::bulk_g2s(sm + dst_off, rec_of(ch) + src_off, bytes, bar);
-        };
-        auto landed = [&](uint64_t* bar) { pend_mask &= ~(1u << (uint32_t)(bar - bar0)); };
         auto w_off = [](uint32_t b) { return b ? kSmW1 : TcRec::W; };
         auto ug_off = [](uint32_t b) { return b ? kSmUG1 : TcRec::U; };
         if (tid == 0) {
             load(&bars->w[0], TcRec::W, TcRec::W, 32768, c_begin);
             load(&bars->ug[0], TcRec::U, TcRec::U, kUGBytes, c_begin);
-            load(&bars->p, TcRec::P, TcRec::P, 16384, c_begin);
             load(&bars->kt, TcRec::KT, TcRec::KT, 32768, c_begin);
-            load(&bars->qb, TcRec::QB, TcRec::QB, 32768, c_begin);
             if (c_begin + 1 < c_end) {
                 load(&bars->w[1], kSmW1, TcRec::W, 32768, c_begin + 1);
                 load(&bars->ug[1], kSmUG1, TcRec::U, kUGBytes, c_begin + 1);
             }
         }
 
-        // entry state: row v of S^T = pool[slot][h][v][:]
+        // entry state: row v of S^T = pool[slot][h][v][:]; its tf32 copy -> buffer 0
         float S[D];
         const float* Sg = a.pool + ((size_t)slot * H + h) * (size_t)D * D + (size_t)tid * D;
 #pragma unroll
@@ -858,108 +898,98 @@ __global__ void __launch_bounds__(256, 1) chunk_state_tc_kernel(const StateArgs 
         tc::tc_fence_before();
         chain_sync();
 
-        const uint32_t sQB = tc::smem_u32(sm + TcRec::QB);
-        const uint32_t sP = tc::smem_u32(sm + TcRec::P), sKT = tc::smem_u32(sm + TcRec::KT);
-        constexpr uint32_t kId64 = tc::idesc_tf32(128, 64), kId128 = tc::idesc_tf32(128, 128);
+        const uint32_t sKT = tc::smem_u32(sm + TcRec::KT);
         bool ok = true;
-        float* s_gl = reinterpret_cast<float*>(sm + kSmBars + sizeof(TcBars) + 32);  // e^{G_L} of the chunk
-
         for (int64_t ch = c_begin; ch < c_end; ++ch) {
             const uint32_t i = (uint32_t)(ch - c_begin);
             const uint32_t ph = i & 1u, b = i & 1u, phb = (i >> 1) & 1u;
             const float* sU = reinterpret_cast<const float*>(sm + ug_off(b));
             const float* sG = sU + 32768 / 4;
 
-            // (a)
+            // (a): Dd is the previous chunk's Delta^T, free once its (b2) is done
             if (tid == 0) {
                 tc::tc_fence_after();
-                ok = tc::mbar_wait(&bars->w[b], phb, kWaitPolls) && ok;
-                if (ok) landed(&bars->w[b]);
-                const uint32_t sW = tc::smem_u32(sm + w_off(b));
+                ok = wait(&bars->w[b], phb) && (i == 0 || wait(&bars->b2_done, (i - 1) & 1u)) && ok;
+                if (ok) {
+                    landed(&bars->w[b]);
+                    tc::tc_fence_after();
+                    const uint32_t sW = tc::smem_u32(sm + w_off(b));
 #pragma unroll
-                for (int s = 0; s < D / 8; ++s)
-                    tc::mma_tf32_ts(tmem + kT_DD, tmem + kT_SOP + 8 * s, tc::smem_desc(sW + 256 * s, 128, 4096), kId64, s > 0);
-                tc::mma_commit(&bars->mma_a);
-                if (!ok) *s_abort = 1;
+                    for (int s = 0; s < D / 8; ++s)
+                        tc::mma_tf32_ts(tmem + kT_DD, tmem + kT_SOP + 128 * b + 8 * s, tc::smem_desc(sW + 256 * s, 128, 4096),
+                                        kId64, s > 0);
+                    tc::mma_commit(&bars->mma_a);
+                }
             }
-            // Delta^T = U^T - S^T W^T, rounded copy to TMEM
+            // Delta^T = U^T - S^T W^T, rounded, over Dd
             {
-                const bool okw = tc::mbar_wait(&bars->ug[b], phb, kWaitPolls) && tc::mbar_wait(&bars->mma_a, ph, kWaitPolls);
-                if (!okw) *s_abort = 1;
+                const bool okw = wait(&bars->ug[b], phb) && wait(&bars->mma_a, ph);
                 if (okw && tid == 0) landed(&bars->ug[b]);
                 tc::tc_fence_after();
+                if (okw) {
 #pragma unroll
-                for (int r0 = 0; r0 < C; r0 += 16) {
-                    float d[16];
-                    tc::tmem_ld16(tmem + lane + kT_DD + r0, d);
+                    for (int r0 = 0; r0 < C; r0 += 16) {
+                        float d[16];
+                        tc::tmem_ld16(tmem + lane + kT_DD + r0, d);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) d[j] = tc::round_tf32(sU[(r0 + j) * D + tid] - d[j]);
-                    tc::tmem_st16_nowait(tmem + lane + kT_DOP + r0, d);
+                        for (int j = 0; j < 16; ++j) d[j] = tc::round_tf32(sU[(r0 + j) * D + tid] - d[j]);
+                        tc::tmem_st16_nowait(tmem + lane + kT_DD + r0, d);
+                    }
+                    s_gl[tid] = sG[tid];                 // the buffer is refilled before (c) retires
+                    tc::tmem_wait_st();
                 }
-                s_gl[tid] = sG[tid];                     // the buffer is refilled before (c) retires
-                tc::tmem_wait_st();
             }
             tc::tc_fence_before();
             chain_sync();
             if (*s_abort) break;
-            // refill W and U/gL of buffer b with chunk i + 2; (b2), (c), (b)
+            // Delta ready for (b2); refill W and U/gL of buffer b with chunk i + 2; (c)
             if (tid == 0) {
                 tc::tc_fence_after();
+                tc::mbar_arrive(&bars->delta_ready);
                 if (ch + 2 < c_end) {
                     load(&bars->w[b], w_off(b), TcRec::W, 32768, ch + 2);
                     load(&bars->ug[b], ug_off(b), TcRec::U, kUGBytes, ch + 2);
                 }
-                const uint32_t tout = tmem + kT_OUT + 64 * (i & 1u);
-                if (i >= 2) ok = tc::mbar_wait(&bars->out_free[i & 1u], ((i - 2) >> 1) & 1u, kWaitPolls) && ok;
-                ok = tc::mbar_wait(&bars->p, ph, kWaitPolls) && ok;
-                if (ok) landed(&bars->p);
-                tc::tc_fence_after();
+                ok = wait(&bars->kt, ph) && ok;
+                if (ok) {
+                    landed(&bars->kt);
+                    tc::tc_fence_after();
 #pragma unroll
-                for (int s = 0; s < C / 8; ++s)
-                    tc::mma_tf32_ts(tout, tmem + kT_DOP + 8 * s, tc::smem_desc(sP + 256 * s, 128, 2048), kId64, s > 0);
-                ok = tc::mbar_wait(&bars->kt, ph, kWaitPolls) && ok;
-                if (ok) landed(&bars->kt);
-#pragma unroll
-                for (int s = 0; s < C / 8; ++s)
-                    tc::mma_tf32_ts(tmem + kT_SC, tmem + kT_DOP + 8 * s, tc::smem_desc(sKT + 256 * s, 128, 2048), kId128, s > 0);
-                ok = tc::mbar_wait(&bars->qb, ph, kWaitPolls) && ok;
-                if (ok) landed(&bars->qb);
-#pragma unroll
-                for (int s = 0; s < D / 8; ++s)
-                    tc::mma_tf32_ts(tout, tmem + kT_SOP + 8 * s, tc::smem_desc(sQB + 256 * s, 128, 4096), kId64, 1);
-                tc::mma_commit(&bars->mma_c);
-                tc::mma_commit(&bars->out_ready[i & 1u]);
-                if (!ok) *s_abort = 1;
+                    for (int s = 0; s < C / 8; ++s)
+                        tc::mma_tf32_ts(tmem + kT_SC, tmem + kT_DD + 8 * s, tc::smem_desc(sKT + 256 * s, 128, 2048), kId128, s > 0);
+                    tc::mma_commit(&bars->mma_c);
+                }
             }
-            // S^T <- S^T Diag(e^{G_L}) + Delta^T Ktil; refresh the tf32 copy
+            // S^T <- S^T Diag(e^{G_L}) + Delta^T Ktil; tf32 copy -> buffer (i + 1) & 1, which (b) of
+            // chunk i - 1 reads
             {
-                if (!tc::mbar_wait(&bars->mma_c, ph, kWaitPolls)) *s_abort = 1;
+                bool okc = wait(&bars->mma_c, ph);
+                if (okc && i >= 1) okc = wait(&bars->out_ready[(i - 1) & 1u], ((i - 1) >> 1) & 1u);
                 tc::tc_fence_after();
-                if (tid == 0 && ch + 1 < c_end && !*s_abort) {  // P, Ktil^T, Qbar of the next chunk
-                    load(&bars->p, TcRec::P, TcRec::P, 16384, ch + 1);
-                    load(&bars->kt, TcRec::KT, TcRec::KT, 32768, ch + 1);
-                    load(&bars->qb, TcRec::QB, TcRec::QB, 32768, ch + 1);
-                }
+                if (okc && tid == 0 && ch + 1 < c_end) load(&bars->kt, TcRec::KT, TcRec::KT, 32768, ch + 1);
+                if (okc) {
+                    const uint32_t sop = kT_SOP + 128 * (b ^ 1u);
 #pragma unroll
-                for (int c = 0; c < D; c += 16) {
-                    float d[16];
-                    tc::tmem_ld16(tmem + lane + kT_SC + c, d);
+                    for (int c = 0; c < D; c += 16) {
+                        float d[16];
+                        tc::tmem_ld16(tmem + lane + kT_SC + c, d);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        S[c + j] = fmaf(S[c + j], s_gl[c + j], d[j]);
-                        d[j] = tc::round_tf32(S[c + j]);
+                        for (int j = 0; j < 16; ++j) {
+                            S[c + j] = fmaf(S[c + j], s_gl[c + j], d[j]);
+                            d[j] = tc::round_tf32(S[c + j]);
+                        }
+                        tc::tmem_st16_nowait(tmem + lane + sop + c, d);
                     }
-                    tc::tmem_st16_nowait(tmem + lane + kT_SOP + c, d);
-                }
-                tc::tmem_wait_st();
-                if (a.snap) {                            // state after this chunk
-                    if (ch < a.snap_cap) {
-                        float* Sd = a.snap + (((size_t)ch * H + h) * D + tid) * (size_t)D;
+                    tc::tmem_wait_st();
+                    if (a.snap) {                        // state after this chunk
+                        if (ch < a.snap_cap) {
+                            float* Sd = a.snap + (((size_t)ch * H + h) * D + tid) * (size_t)D;
 #pragma unroll
-                        for (int c = 0; c < D; c += 4)
-                            *reinterpret_cast<float4*>(Sd + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
-                    } else if (tid == 0) {
-                        record_error(kDevErrSeqlens);
+                            for (int c = 0; c < D; c += 4)
+                                *reinterpret_cast<float4*>(Sd + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+                        } else if (tid == 0) {
+                            record_error(kDevErrSeqlens);
+                        }
                     }
                 }
             }
@@ -967,16 +997,11 @@ __global__ void __launch_bounds__(256, 1) chunk_state_tc_kernel(const StateArgs 
             chain_sync();
             if (*s_abort) break;
         }
-
         if (*s_abort) {
-            // A wait gave up: record it, let every MMA this CTA issued and every copy still in flight
-            // land (bounded waits).  The slot is left as it was.
+            // A wait gave up: record it, let this side's MMAs and copies land.  The slot is left as it was.
             if (tid == 0) {
                 record_error(kDevErrTimeout);
-                tc::mma_commit(&bars->drain);
-                tc::mbar_wait(&bars->drain, 0, kWaitPolls);
-                for (uint32_t bi = 0; bi < 7; ++bi)
-                    if (pend_mask & (1u << bi)) tc::mbar_wait(bar0 + bi, (pend_par >> bi) & 1u, kWaitPolls);
+                drain(&bars->drain[0]);
             }
         } else {
             float* Sd = a.pool + ((size_t)slot * H + h) * (size_t)D * D + (size_t)tid * D;
