@@ -681,24 +681,27 @@ __global__ void __launch_bounds__(256, 1) chunk_state_kernel(const StateArgs a)
 }
 
 // ---- inter-chunk state pass on the tensor cores (C = 64, D = 128) --------------------------------
-// One CTA of 256 threads per (sequence, head), in the transposed ("value-major") form so that every
+// One CTA of 384 threads per (sequence, head), in the transposed ("value-major") form so that every
 // MMA has M = 128 rows = the 128 value rows (TMEM lane v).  Per chunk:
 //   (a)  Dd   = S^T W^T                  A = tf32 copy of S^T in TMEM, B = W image       (N = 64)
-//   chain threads: Delta^T = U^T - Dd, rounded to tf32, written over Dd
+//   Delta^T = U^T - Dd, rounded to tf32, written over Dd
 //   (c)  Dc   = Delta^T Ktil             A = Delta^T in TMEM,          B = Ktil^T image  (N = 128)
-//   chain threads: S^T <- S^T Diag(e^{G_L}) + Dc (fp32 in registers), tf32 copy to the other buffer
+//   S^T <- S^T Diag(e^{G_L}) + Dc (fp32 in registers), its tf32 copy into the other TMEM buffer
 //   (b2) Do   = Delta^T P^T              A = Delta^T,                  B = P image       (N = 64)
 //   (b)  Do  += S^T Qbar^T               A = S^T (this chunk's copy),  B = Qbar image    (N = 64)
-//   output threads: O^T = Do -> out
-// Warps 0..3 run the serial chain ((a), Delta, (c), S update): thread v owns value row v of S^T in
-// registers.  Warps 4..7 produce the output: thread 128 issues (b2) and (b) once Delta is ready and
-// P / Qbar have landed, and the four warps copy Do to the output, so neither the output MMAs nor
-// their operands (P, Qbar) sit on the chain.  The S^T copy is double-buffered (chunk i reads buffer
-// i & 1), so the S update of chunk i only waits for (b) of chunk i - 1.  Hand-offs: mbarriers
-// (delta_ready: chain -> issuer; b2_done, out_ready[2]: tensor-core commits of the issuer).
-// Operand images arrive by bulk async copy from the record: W and U/gL double-buffered (two chunks
-// ahead), Ktil^T, P and Qbar one chunk ahead.  All waits are bounded and give up early once either
-// side has recorded a failure.
+//   O^T = Do -> out
+// Warps 0..7 share the chain: thread v of warp group g (0: warps 0..3, 1: warps 4..7) is TMEM
+// lane v and owns columns 64 g .. 64 g + 63 of row v of S^T in registers; each group computes half
+// of Delta (rows r = 32 g ..) and half of the S update.  Thread 0 issues (a) and (c) and loads W,
+// U/gL and Ktil^T.  Warps 8..11 produce the output: thread 256 issues (b2) and (b) once Delta is
+// ready and P / Qbar have landed, and loads P and Qbar; the four warps copy Do to the output.
+// Neither the output MMAs, their operands nor the output stores sit on the chain.  The S^T copy is
+// double-buffered (chunk i reads buffer i & 1), so the S update of chunk i only waits for (b) of
+// chunk i - 1.  Hand-offs are mbarriers (delta_ready: an arrival of thread 0; b2_done,
+// out_ready[2]: tensor-core commits of thread 256).  Operand images arrive by bulk async copy from
+// the record: W and U/gL double-buffered (two chunks ahead), Ktil^T, P and Qbar one chunk ahead.
+// All waits are bounded and give up early once any thread has recorded a failure; loop exits are
+// made uniform with barrier reductions.
 constexpr uint32_t kWaitPolls = 1u << 24;
 
 // shared memory: the record image (one buffer set) followed by the second W and U/gL buffers
@@ -708,9 +711,9 @@ constexpr uint32_t kUGBytes = 32768 + 512;
 constexpr uint32_t kSmBars = kSmUG1 + kUGBytes;
 struct TcBars {
     uint64_t w[2], ug[2], kt, qb, p;  // operand buffers filled (tx bytes); these seven come first
-    uint64_t mma_a;                   // (a) complete                    (chain commit)
-    uint64_t mma_c;                   // (c) complete                    (chain commit)
-    uint64_t delta_ready;             // Delta^T of the chunk is in TMEM (chain thread 0 arrives)
+    uint64_t mma_a;                   // (a) complete                    (thread 0 commit)
+    uint64_t mma_c;                   // (c) complete                    (thread 0 commit)
+    uint64_t delta_ready;             // Delta^T of the chunk is in TMEM (thread 0 arrives)
     uint64_t b2_done;                 // (b2) complete: Delta^T may be overwritten (issuer commit)
     uint64_t out_ready[2];            // (b) of chunk i complete, Do ready; index i & 1 (issuer commit)
     uint64_t drain[2];                // used once each, to drain the tensor core after a failed wait
@@ -718,6 +721,7 @@ struct TcBars {
 constexpr size_t kTcSmemBytes = kSmBars + 1024;
 static_assert(sizeof(TcBars) + 32 + 512 <= 1024, "barriers, TMEM base, abort flag and e^{G_L}");
 static_assert(kTcSmemBytes <= 232448, "state-pass shared memory");
+constexpr int kStateThreads = 384;
 
 // TMEM column map (512 columns allocated; each accumulator starts at a multiple of its width)
 constexpr uint32_t kT_SOP = 0;     // tf32 S^T, two buffers   (2 x 128 cols, A operand)
@@ -725,13 +729,31 @@ constexpr uint32_t kT_SC = 256;    // Delta^T Ktil            (128, accumulator)
 constexpr uint32_t kT_DD = 384;    // S^T W^T, then Delta^T   (64, accumulator, then A operand)
 constexpr uint32_t kT_OUT = 448;   // O^T                     (64, accumulator)
 
-__device__ __forceinline__ void chain_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-__device__ __forceinline__ void output_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+__device__ __forceinline__ void chain_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Named barrier that also returns, to every participating thread, whether any of them passed a
+// true flag: a loop exit after a failure is uniform even though the failure flag is written
+// asynchronously by other warps.  Barrier 1: the 256 chain threads; barrier 2: the 128 output threads.
+template <int ID, int COUNT>
+__device__ __forceinline__ bool sync_any(bool flag)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)flag), "n"(ID), "n"(COUNT)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ bool chain_sync_any(bool flag) { return sync_any<1, 256>(flag); }
+__device__ __forceinline__ bool output_sync_any(bool flag) { return sync_any<2, 128>(flag); }
 
 template <typename TOut>
-__global__ void __launch_bounds__(256, 1) chunk_state_tc_kernel(const StateArgs a)
+__global__ void __launch_bounds__(kStateThreads, 1) chunk_state_tc_kernel(const StateArgs a)
 {
-    constexpr int C = TcRec::C, D = TcRec::D;
+    constexpr int C = TcRec::C, D = TcRec::D, DH = D / 2;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = smem_raw;
     TcBars* bars = reinterpret_cast<TcBars*>(sm + kSmBars);
@@ -780,7 +802,7 @@ __global__ void __launch_bounds__(256, 1) chunk_state_tc_kernel(const StateArgs 
     const uint32_t tmem = *s_taddr;
     const uint32_t lane = (uint32_t)((warp & 3) * 32) << 16;
 
-    // bounded wait that also gives up once the other side has recorded a failure
+    // bounded wait that also gives up once any thread has recorded a failure
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
         for (uint32_t it = 0; it < kWaitPolls; ++it) {
             if (tc::mbar_try_wait(bar, parity)) return true;
@@ -812,9 +834,9 @@ __global__ void __launch_bounds__(256, 1) chunk_state_tc_kernel(const StateArgs 
     };
     constexpr uint32_t kId64 = tc::idesc_tf32(128, 64), kId128 = tc::idesc_tf32(128, 128);
 
-    if (warp >= 4) {
-        // ---- output side: thread 128 issues (b2) and (b); warps 4..7 copy Do to the output
-        const int v = tid - 128;
+    if (warp >= 8) {
+        // ---- output side: thread 256 issues (b2) and (b); warps 8..11 copy Do to the output
+        const int v = tid - 256;
         const bool issuer = (v == 0);
         const uint32_t sQB = tc::smem_u32(sm + TcRec::QB), sP = tc::smem_u32(sm + TcRec::P);
         if (issuer) {
@@ -822,7 +844,7 @@ __global__ void __launch_bounds__(256, 1) chunk_state_tc_kernel(const StateArgs 
             load(&bars->qb, TcRec::QB, TcRec::QB, 32768, c_begin);
         }
         bool ok = true;
-        for (int64_t ch = c_begin; ch < c_end && ok; ++ch) {
+        for (int64_t ch = c_begin; ch < c_end; ++ch) {
             const uint32_t i = (uint32_t)(ch - c_begin), ph = i & 1u;
             if (issuer) {
                 ok = wait(&bars->delta_ready, ph) && wait(&bars->p, ph);
@@ -844,29 +866,32 @@ __global__ void __launch_bounds__(256, 1) chunk_state_tc_kernel(const StateArgs 
                     tc::mma_commit(&bars->out_ready[i & 1u]);
                 }
             }
-            ok = wait(&bars->out_ready[i & 1u], (i >> 1) & 1u);   // every output thread
-            if (!ok) break;
-            tc::tc_fence_after();
-            if (issuer && ch + 1 < c_end) {            // (b2) and (b) are done with P and Qbar
-                load(&bars->p, TcRec::P, TcRec::P, 16384, ch + 1);
-                load(&bars->qb, TcRec::QB, TcRec::QB, 32768, ch + 1);
-            }
-            const int64_t t0 = a.chunk_start[ch];
-            const int L = a.chunk_len[ch];
+            const bool okr = ok && wait(&bars->out_ready[i & 1u], (i >> 1) & 1u);   // every output thread
+            if (okr) {
+                tc::tc_fence_after();
+                if (issuer && ch + 1 < c_end) {          // (b2) and (b) are done with P and Qbar
+                    load(&bars->p, TcRec::P, TcRec::P, 16384, ch + 1);
+                    load(&bars->qb, TcRec::QB, TcRec::QB, 32768, ch + 1);
+                }
+                const int64_t t0 = a.chunk_start[ch];
+                const int L = a.chunk_len[ch];
 #pragma unroll
-            for (int r0 = 0; r0 < C; r0 += 16) {
-                float o[16];
-                tc::tmem_ld16(tmem + lane + kT_OUT + r0, o);
+                for (int r0 = 0; r0 < C; r0 += 16) {
+                    float o[16];
+                    tc::tmem_ld16(tmem + lane + kT_OUT + r0, o);
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    if (r0 + j < L) out[((size_t)(t0 + r0 + j) * H + h) * D + v] = from_f32<TOut>(o[j]);
+                    for (int j = 0; j < 16; ++j)
+                        if (r0 + j < L) out[((size_t)(t0 + r0 + j) * H + h) * D + v] = from_f32<TOut>(o[j]);
+                }
             }
             tc::tc_fence_before();
-            output_sync();                             // Do is free for the next chunk's (b2)
+            if (output_sync_any(!okr || *s_abort != 0)) break;   // Do is free for the next (b2)
         }
         if (issuer && *s_abort) drain(&bars->drain[1]);
+        __syncwarp();
     } else {
-        // ---- the chain (warps 0..3)
+        // ---- the chain: warp group g = warp >> 2 owns S^T columns 64 g .. 64 g + 63 of row v
+        const int g = warp >> 2, v = tid & (D - 1);
         auto w_off = [](uint32_t b) { return b ? kSmW1 : TcRec::W; };
         auto ug_off = [](uint32_t b) { return b ? kSmUG1 : TcRec::U; };
         if (tid == 0) {
@@ -879,20 +904,20 @@ __global__ void __launch_bounds__(256, 1) chunk_state_tc_kernel(const StateArgs 
             }
         }
 
-        // entry state: row v of S^T = pool[slot][h][v][:]; its tf32 copy -> buffer 0
-        float S[D];
-        const float* Sg = a.pool + ((size_t)slot * H + h) * (size_t)D * D + (size_t)tid * D;
+        // entry state: columns 64 g .. of row v of S^T = pool[slot][h][v][:]; tf32 copy -> buffer 0
+        float S[DH];
+        const float* Sg = a.pool + ((size_t)slot * H + h) * (size_t)D * D + (size_t)v * D + DH * g;
 #pragma unroll
-        for (int c = 0; c < D; c += 4) {
+        for (int c = 0; c < DH; c += 4) {
             const float4 x = *reinterpret_cast<const float4*>(Sg + c);
             S[c] = x.x; S[c + 1] = x.y; S[c + 2] = x.z; S[c + 3] = x.w;
         }
 #pragma unroll
-        for (int c = 0; c < D; c += 16) {
+        for (int c = 0; c < DH; c += 16) {
             float t[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) t[j] = tc::round_tf32(S[c + j]);
-            tc::tmem_st16_nowait(tmem + lane + kT_SOP + c, t);
+            tc::tmem_st16_nowait(tmem + lane + kT_SOP + DH * g + c, t);
         }
         tc::tmem_wait_st();
         tc::tc_fence_before();
@@ -921,29 +946,27 @@ __global__ void __launch_bounds__(256, 1) chunk_state_tc_kernel(const StateArgs 
                     tc::mma_commit(&bars->mma_a);
                 }
             }
-            // Delta^T = U^T - S^T W^T, rounded, over Dd
+            // Delta^T = U^T - S^T W^T (rows r = 32 g .. 32 g + 31), rounded, over Dd
             {
                 const bool okw = wait(&bars->ug[b], phb) && wait(&bars->mma_a, ph);
                 if (okw && tid == 0) landed(&bars->ug[b]);
                 tc::tc_fence_after();
                 if (okw) {
 #pragma unroll
-                    for (int r0 = 0; r0 < C; r0 += 16) {
+                    for (int r0 = 32 * g; r0 < 32 * g + 32; r0 += 16) {
                         float d[16];
                         tc::tmem_ld16(tmem + lane + kT_DD + r0, d);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) d[j] = tc::round_tf32(sU[(r0 + j) * D + tid] - d[j]);
+                        for (int j = 0; j < 16; ++j) d[j] = tc::round_tf32(sU[(r0 + j) * D + v] - d[j]);
                         tc::tmem_st16_nowait(tmem + lane + kT_DD + r0, d);
                     }
-                    s_gl[tid] = sG[tid];                 // the buffer is refilled before (c) retires
+                    if (g == 0) s_gl[v] = sG[v];         // the buffer is refilled before (c) retires
                     tc::tmem_wait_st();
                 }
             }
             tc::tc_fence_before();
-            chain_sync();
-            if (*s_abort) break;
-            // Delta ready for (b2); refill W and U/gL of buffer b with chunk i + 2; (c)
-            if (tid == 0) {
+            if (chain_sync_any(*s_abort != 0)) break;
+            if (tid == 0) {                              // Delta ready; refill W, U/gL(b); (c)
                 tc::tc_fence_after();
                 tc::mbar_arrive(&bars->delta_ready);
                 if (ch + 2 < c_end) {
@@ -960,22 +983,22 @@ __global__ void __launch_bounds__(256, 1) chunk_state_tc_kernel(const StateArgs 
                     tc::mma_commit(&bars->mma_c);
                 }
             }
-            // S^T <- S^T Diag(e^{G_L}) + Delta^T Ktil; tf32 copy -> buffer (i + 1) & 1, which (b) of
-            // chunk i - 1 reads
+            // S^T <- S^T Diag(e^{G_L}) + Delta^T Ktil on this group's columns; tf32 copy -> buffer
+            // (i + 1) & 1, which (b) of chunk i - 1 reads
             {
                 bool okc = wait(&bars->mma_c, ph);
                 if (okc && i >= 1) okc = wait(&bars->out_ready[(i - 1) & 1u], ((i - 1) >> 1) & 1u);
                 tc::tc_fence_after();
                 if (okc && tid == 0 && ch + 1 < c_end) load(&bars->kt, TcRec::KT, TcRec::KT, 32768, ch + 1);
                 if (okc) {
-                    const uint32_t sop = kT_SOP + 128 * (b ^ 1u);
+                    const uint32_t sop = kT_SOP + 128 * (b ^ 1u) + DH * g;
 #pragma unroll
-                    for (int c = 0; c < D; c += 16) {
+                    for (int c = 0; c < DH; c += 16) {
                         float d[16];
-                        tc::tmem_ld16(tmem + lane + kT_SC + c, d);
+                        tc::tmem_ld16(tmem + lane + kT_SC + DH * g + c, d);
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            S[c + j] = fmaf(S[c + j], s_gl[c + j], d[j]);
+                            S[c + j] = fmaf(S[c + j], s_gl[DH * g + c + j], d[j]);
                             d[j] = tc::round_tf32(S[c + j]);
                         }
                         tc::tmem_st16_nowait(tmem + lane + sop + c, d);
@@ -983,9 +1006,9 @@ __global__ void __launch_bounds__(256, 1) chunk_state_tc_kernel(const StateArgs 
                     tc::tmem_wait_st();
                     if (a.snap) {                        // state after this chunk
                         if (ch < a.snap_cap) {
-                            float* Sd = a.snap + (((size_t)ch * H + h) * D + tid) * (size_t)D;
+                            float* Sd = a.snap + (((size_t)ch * H + h) * D + v) * (size_t)D + DH * g;
 #pragma unroll
-                            for (int c = 0; c < D; c += 4)
+                            for (int c = 0; c < DH; c += 4)
                                 *reinterpret_cast<float4*>(Sd + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
                         } else if (tid == 0) {
                             record_error(kDevErrSeqlens);
@@ -994,20 +1017,21 @@ __global__ void __launch_bounds__(256, 1) chunk_state_tc_kernel(const StateArgs 
                 }
             }
             tc::tc_fence_before();
-            chain_sync();
-            if (*s_abort) break;
+            if (chain_sync_any(*s_abort != 0)) break;
         }
-        if (*s_abort) {
+        const bool aborted = chain_sync_any(*s_abort != 0);
+        if (aborted) {
             // A wait gave up: record it, let this side's MMAs and copies land.  The slot is left as it was.
             if (tid == 0) {
                 record_error(kDevErrTimeout);
                 drain(&bars->drain[0]);
             }
         } else {
-            float* Sd = a.pool + ((size_t)slot * H + h) * (size_t)D * D + (size_t)tid * D;
+            float* Sd = a.pool + ((size_t)slot * H + h) * (size_t)D * D + (size_t)v * D + DH * g;
 #pragma unroll
-            for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(Sd + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+            for (int c = 0; c < DH; c += 4) *reinterpret_cast<float4*>(Sd + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
         }
+        __syncwarp();
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -1412,6 +1436,16 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
     }
     __syncthreads();
 
+    // value loads for (beta V)^T (lane v, columns j = 32 jh ..), issued here so that their latency
+    // overlaps the Gram operands; consumed after the Gram completes
+    const int vv_ = tid & (D - 1), jh = tid >> 7;
+    float vr[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int j = 32 * jh + i;
+        vr[i] = j < L ? __bfloat162float(vp[((size_t)(t0 + j) * H + h) * D + vv_]) : 0.f;
+    }
+
     // 4. Gram operands and the Qbar record.  B image chunk f (16 bytes = 8 fp16 of one row) sits at
     //    byte 16 f: core (n >> 3, c >> 3) = f >> 3, row n & 7 = f & 7; rows n = 32 (I - 1) + {0..15:
     //    k o Rin, 16..31: q o Rin} of row block I.  Read now, written over the q tile after a barrier.
@@ -1475,14 +1509,7 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
         tc::mma_commit(bar_g);
     }
 
-    // 5. value loads for (beta V)^T (lane v, columns j = 32 jh ..), then the Gram result
-    const int vv_ = tid & (D - 1), jh = tid >> 7;
-    float vr[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const int j = 32 * jh + i;
-        vr[i] = j < L ? __bfloat162float(vp[((size_t)(t0 + j) * H + h) * D + vv_]) : 0.f;
-    }
+    // 5. the Gram result; (beta V)^T from the values loaded before the Gram operands
     {
         const bool done = tc::mbar_wait(bar_g, 0, kWaitPolls);
         tc::tc_fence_after();
@@ -1676,7 +1703,7 @@ cudaError_t run_prefill(const kda_params& p, const GateParams& gp, const void* q
         auto state = chunk_state_tc_kernel<TOut>;
         e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmemBytes);
         if (e != cudaSuccess) return e;
-        state<<<(unsigned)((int64_t)N * H), 256, kTcSmemBytes, stream>>>(sa);
+        state<<<(unsigned)((int64_t)N * H), kStateThreads, kTcSmemBytes, stream>>>(sa);
     } else {
         constexpr int NV = D < 32 ? D : 32;
         using SS = StateShape<C, D, NV>;
