@@ -60,6 +60,28 @@ def test_chunk_and_dim_grid(C, D, io):
     check(inp, H, D, C, io)
 
 
+@pytest.mark.parametrize("io,C,D", [(torch.bfloat16, 64, 128), (torch.float32, 16, 32)])
+def test_many_short_sequences(io, C, D):
+    """4300 sequences (more than the 4096 the chunk table orders by length, so the state pass takes
+    them in index order), lengths cycling through 0..5 tokens after a few multi-chunk ones, every
+    sequence in its own slot; a quarter of them padding."""
+    lengths = [130, 65, 64] + [(0, 1, 2, 3, 5)[i % 5] for i in range(4297)]
+    N, H = len(lengths), 1
+    pad = tuple(range(7, N, 4))
+    inp = workloads.make_inputs(lengths, H, D, io, pool_slots=N, pool_std=0.05, seed=91, dt_bias_std=0.3,
+                                padding_rows=pad)
+    out, pool = run_prefill(inp, C)
+    o_ref, p_ref, _ = oracle_run(inp, H, D)
+    cu = inp["cu_seqlens"].tolist()
+    live = np.ones(cu[-1], dtype=bool)
+    for b in pad:
+        live[cu[b]:cu[b + 1]] = False
+    got = np64(out)
+    assert rel_err(got[live], o_ref[live]) <= tol_for(io, torch.float32)
+    assert np.all(got[~live] == 0)                                  # padding rows: zero output
+    assert rel_err(np64(pool), p_ref) <= tol_for(io, torch.float32)
+
+
 def test_padding_rows_and_untouched_slots():
     H, D = 2, 64
     inp = workloads.make_inputs([20, 70, 3], H, D, torch.float32, pool_slots=6, pool_std=0.1, seed=3,
