@@ -59,6 +59,14 @@ struct RecArgs {
 
 enum { kModeDecode = 0, kModeVerify = 1, kModeReplay = 2 };
 
+// 16-byte asynchronous copy global -> shared (both addresses 16-byte aligned), bypassing L1
+__device__ __forceinline__ void cp_async16(void* dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+}
+
 template <int D>
 struct RecShape {
     static constexpr int NWARPS = D >= 32 ? D / 16 : 1;
@@ -75,8 +83,9 @@ struct RecShape {
 
 // GATE: KDA_GATE_PER_CHANNEL or KDA_GATE_PER_HEAD.  MODE: kModeDecode updates the pool slot in
 // place; kModeVerify writes every intermediate state to `inter` and leaves the pool untouched;
-// kModeReplay rebuilds the state from the slot's checkpoint and ring, then either appends this
-// step to the ring or (flush) writes the new state to the checkpoint.
+// kModeReplay either appends this step to the ring, computing the outputs from the checkpoint and
+// the committed entries without materializing the state (readout decomposition), or (flush)
+// rebuilds the state from the checkpoint and ring and writes the new state to the checkpoint.
 template <int D, int GATE, int MODE, typename TIn, typename TOut>
 __global__ void __launch_bounds__(RecShape<D>::THREADS, (D >= 128 ? 2 : 4))
 recurrent_kernel(const RecArgs a)
@@ -140,6 +149,23 @@ recurrent_kernel(const RecArgs a)
     float* s_al = s_q + T * D;                           // [T][D] alpha (per-channel gate)
     float* s_v = s_al + T * D;                           // [T][D] v
     float* s_sc = s_v + T * D;                           // [T][8]: beta, q.k, alpha (per head), 1/|k|, scale/|q|
+    if (MODE == kModeReplay && wp > 0) {
+        // the committed ring entries travel to shared memory (asynchronous 16-byte copies) while
+        // the state loads and the prologue proceed
+        float* s_rk = s_sc + 8 * T;
+        float* s_rd = s_rk + a.ring_len * D;
+        float* s_ra = s_rd + a.ring_len * D;
+        const size_t rb = ((size_t)slot * H + h) * (size_t)a.ring_len;
+        const float4* gk = reinterpret_cast<const float4*>(a.ring_k + rb * D);
+        const float4* gd = reinterpret_cast<const float4*>(a.ring_d + rb * D);
+        const float4* ga = reinterpret_cast<const float4*>(a.ring_a + rb * D);
+        for (int e = tid; e < wp * D / 4; e += Sh::THREADS) {
+            cp_async16(reinterpret_cast<float4*>(s_rk) + e, gk + e);
+            cp_async16(reinterpret_cast<float4*>(s_rd) + e, gd + e);
+            if (GATE == KDA_GATE_PER_CHANNEL) cp_async16(reinterpret_cast<float4*>(s_ra) + e, ga + e);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
     const TIn* qp = reinterpret_cast<const TIn*>(a.q);
     const TIn* kp = reinterpret_cast<const TIn*>(a.k);
     const TIn* vp = reinterpret_cast<const TIn*>(a.v);
@@ -198,21 +224,12 @@ recurrent_kernel(const RecArgs a)
         float* s_rd = s_rk + a.ring_len * D;      // [L][D]
         float* s_ra = s_rd + a.ring_len * D;      // [L][D] (per-channel) or [L]
         float* s_tot = s_ra + a.ring_len * D;     // [D]
+        float* s_ck = s_tot + D;                  // [L] k~_j . (a o k_hat)
+        float* s_cq = s_ck + a.ring_len;          // [L] k~_j . (a o q_hat)
         const size_t rb = ((size_t)slot * H + h) * (size_t)a.ring_len;
-        // stage the committed entries with 16-byte loads (all issued before any is used)
-        const float4* gk = reinterpret_cast<const float4*>(a.ring_k + rb * D);
-        const float4* gd = reinterpret_cast<const float4*>(a.ring_d + rb * D);
-        const float4* ga = reinterpret_cast<const float4*>(a.ring_a + rb * D);
-        for (int e = tid; e < wp * D / 4; e += Sh::THREADS) {
-            const float4 k4 = __ldcs(gk + e), d4 = __ldcs(gd + e);
-            float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (GATE == KDA_GATE_PER_CHANNEL) a4 = __ldcs(ga + e);
-            reinterpret_cast<float4*>(s_rk)[e] = k4;
-            reinterpret_cast<float4*>(s_rd)[e] = d4;
-            if (GATE == KDA_GATE_PER_CHANNEL) reinterpret_cast<float4*>(s_ra)[e] = a4;
-        }
         if (GATE == KDA_GATE_PER_HEAD)
             for (int j = tid; j < wp; j += Sh::THREADS) s_ra[j] = a.ring_a[rb + j];
+        asm volatile("cp.async.wait_group 0;" ::: "memory");   // this thread's ring copies
         __syncthreads();
         for (int c = tid; c < D; c += Sh::THREADS) {
             float pr = 1.f;
@@ -223,6 +240,29 @@ recurrent_kernel(const RecArgs a)
             s_tot[c] = pr;
         }
         __syncthreads();
+        if (!flush) {
+            // Readout decomposition (ReplaySSM): with S' = Diag(P) S0 + sum_j k~_j^T d_j, a row of
+            // (a o z) S' is sum_c S0[c] (P o a o z)[c] + sum_j (k~_j . (a o z)) d_j, so a step that
+            // does not flush needs only these dot products and never materializes S'.
+            for (int j = warp; j < wp; j += NWARPS) {
+                float ck = 0.f, cq = 0.f;
+                for (int c = lane; c < D; c += 32) {
+                    const float za = (GATE == KDA_GATE_PER_CHANNEL) ? s_al[c] : s_sc[2];
+                    const float r = s_rk[j * D + c] * za;
+                    ck = fmaf(r, s_k[c], ck);
+                    cq = fmaf(r, s_q[c], cq);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    ck += __shfl_xor_sync(0xffffffffu, ck, off);
+                    cq += __shfl_xor_sync(0xffffffffu, cq, off);
+                }
+                if (lane == 0) {
+                    s_ck[j] = ck;
+                    s_cq[j] = cq;
+                }
+            }
+        } else {
 #pragma unroll
         for (int s = 0; s < STEPS; ++s)
 #pragma unroll
@@ -245,6 +285,7 @@ recurrent_kernel(const RecArgs a)
                     e.x = fmaf(dj[s], kw[j4].x, e.x); e.y = fmaf(dj[s], kw[j4].y, e.y);
                     e.z = fmaf(dj[s], kw[j4].z, e.z); e.w = fmaf(dj[s], kw[j4].w, e.w);
                 }
+        }
         }
     }
     __syncthreads();
@@ -273,6 +314,22 @@ recurrent_kernel(const RecArgs a)
             }
         }
 
+        // replay step that does not flush, with committed entries: the readout decomposition
+        const bool decomp = MODE == kModeReplay && !flush && wp > 0;
+        if (decomp) {                                   // fold P o a into the column constants
+            const float* s_tot = s_sc + 8 * T + (size_t)3 * a.ring_len * D;
+#pragma unroll
+            for (int j = 0; j < NV4; ++j) {
+                const float4 tt = *reinterpret_cast<const float4*>(&s_tot[4 * (li + LPR * j)]);
+                const float pa[4] = {tt.x * al[4 * j + 0], tt.y * al[4 * j + 1], tt.z * al[4 * j + 2], tt.w * al[4 * j + 3]};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    kh[4 * j + u] *= pa[u];
+                    qh[4 * j + u] *= pa[u];
+                }
+            }
+        }
+
         // ---- rows: decay, predict, error, write, read -----------------------------------------
 #pragma unroll
         for (int s = 0; s < STEPS; ++s) {
@@ -282,7 +339,9 @@ recurrent_kernel(const RecArgs a)
 #pragma unroll
             for (int j = 0; j < NV4; ++j) {
                 float4& e = st[s][j];
-                e.x *= al[4 * j + 0]; e.y *= al[4 * j + 1]; e.z *= al[4 * j + 2]; e.w *= al[4 * j + 3];
+                if (!decomp) {
+                    e.x *= al[4 * j + 0]; e.y *= al[4 * j + 1]; e.z *= al[4 * j + 2]; e.w *= al[4 * j + 3];
+                }
                 pk = fmaf(e.x, kh[4 * j + 0], pk); pk = fmaf(e.y, kh[4 * j + 1], pk);
                 pk = fmaf(e.z, kh[4 * j + 2], pk); pk = fmaf(e.w, kh[4 * j + 3], pk);
                 pq = fmaf(e.x, qh[4 * j + 0], pq); pq = fmaf(e.y, qh[4 * j + 1], pq);
@@ -293,13 +352,24 @@ recurrent_kernel(const RecArgs a)
                 pk += __shfl_xor_sync(0xffffffffu, pk, off);
                 pq += __shfl_xor_sync(0xffffffffu, pq, off);
             }
+            if (decomp) {                               // + sum_j (k~_j . (a o z)) d_j[row]
+                const float* s_rd = s_sc + 8 * T + (size_t)a.ring_len * D;
+                const float* s_ck = s_sc + 8 * T + (size_t)3 * a.ring_len * D + D;
+                for (int j = 0; j < wp; ++j) {
+                    const float dj = s_rd[j * D + row];
+                    pk = fmaf(s_ck[j], dj, pk);
+                    pq = fmaf(s_ck[a.ring_len + j], dj, pq);
+                }
+            }
             const float delta = beta * (vj - pk);
             const float o = fmaf(delta, qk, pq);
+            if (!(MODE == kModeReplay && !flush)) {     // a replay step that does not flush keeps S0
 #pragma unroll
-            for (int j = 0; j < NV4; ++j) {
-                float4& e = st[s][j];
-                e.x = fmaf(delta, kh[4 * j + 0], e.x); e.y = fmaf(delta, kh[4 * j + 1], e.y);
-                e.z = fmaf(delta, kh[4 * j + 2], e.z); e.w = fmaf(delta, kh[4 * j + 3], e.w);
+                for (int j = 0; j < NV4; ++j) {
+                    float4& e = st[s][j];
+                    e.x = fmaf(delta, kh[4 * j + 0], e.x); e.y = fmaf(delta, kh[4 * j + 1], e.y);
+                    e.z = fmaf(delta, kh[4 * j + 2], e.z); e.w = fmaf(delta, kh[4 * j + 3], e.w);
+                }
             }
             if (li == 0) out[rowbase + row] = from_f32<TOut>(o);
             if (MODE == kModeReplay && !flush) {      // append d to the ring; the state stays put
@@ -328,10 +398,10 @@ recurrent_kernel(const RecArgs a)
 }
 
 // Dynamic shared memory of one recurrent CTA: four [T][D] tiles and 8 scalars per token, plus in
-// replay mode three [L][D] ring tiles and one [D] vector.
+// replay mode three [L][D] ring tiles, one [D] vector and two [L] vectors.
 inline size_t recurrent_smem_bytes(int D, int T, int L)
 {
-    return sizeof(float) * ((size_t)4 * T * D + 8 * (size_t)T + (size_t)3 * L * D + D);
+    return sizeof(float) * ((size_t)4 * T * D + 8 * (size_t)T + (size_t)3 * L * D + D + (size_t)2 * L);
 }
 
 template <int D, int GATE, int MODE, typename TIn, typename TOut>
