@@ -36,11 +36,11 @@ UNIT = "tokens/s"
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, one ncu capture of a bench
 # step, caches flushed before each kernel), valid only for the kernel source they were taken on.
 MEASURED_TRAFFIC = {
-    "kda_prefill.cu": {"sha256_16": "6f3d99de4721f3f4",
-                       "kda_chunk_table": 0.0, "kda_chunk_intra": 1872.3e6, "kda_chunk_state": 1393.0e6},
-    "kda_recurrent.cu": {"sha256_16": "ba7b6bba8aab7c2f",
-                         "kda_recurrent_decode": 1024.8e6, "kda_recurrent_verify": 614.3e6,
-                         "kda_replay_decode": 624.9e6},
+    "kda_prefill.cu": {"sha256_16": "b785eed2b1ddf472",
+                       "kda_chunk_table": 0.0, "kda_chunk_intra": 1869.6e6, "kda_chunk_state": 1393.6e6},
+    "kda_recurrent.cu": {"sha256_16": "006c0c82c01df777",
+                         "kda_recurrent_decode": 1024.4e6, "kda_recurrent_verify": 614.4e6,
+                         "kda_replay_decode": 620.3e6},
 }
 
 
