@@ -1050,11 +1050,6 @@ __device__ __forceinline__ float4 rnd4(float4 a)
 {
     return make_float4(tc::round_tf32(a.x), tc::round_tf32(a.y), tc::round_tf32(a.z), tc::round_tf32(a.w));
 }
-__device__ __forceinline__ float dot4(float4 a, float4 b, float acc)
-{
-    acc = fmaf(a.x, b.x, acc); acc = fmaf(a.y, b.y, acc); acc = fmaf(a.z, b.z, acc);
-    return fmaf(a.w, b.w, acc);
-}
 __device__ __forceinline__ float ex2_approx(float x)
 {
     float y;
@@ -1081,12 +1076,6 @@ __device__ __forceinline__ float alpha_mufu(float x, float rate, const GateParam
 }
 // Packed fp32 pairs (one 64-bit register pair) and the sm_100+ paired FP32 instructions; each lane
 // of a pair is an ordinary IEEE fp32 multiply / fused multiply-add.
-__device__ __forceinline__ uint64_t f2pack(float x, float y)
-{
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
-    return r;
-}
 __device__ __forceinline__ float f2sum(uint64_t r)
 {
     float x, y;
