@@ -1,4 +1,4 @@
-// kda_prefill.cu -- chunkwise-parallel KDA prefill over packed varlen sequences (fp32 SIMT path).
+// kda_prefill.cu -- chunkwise-parallel KDA prefill over packed varlen sequences.
 //
 // Algorithm ("linear_attention", zdszero.github.io, sections "矩阵（并行）形式" and
 // "两种计算形态"): each sequence is cut into chunks of C tokens.  For a chunk of L tokens with
@@ -11,10 +11,14 @@
 //
 // Three kernels, all on the caller's stream, no host synchronisation:
 //   chunk_table_kernel   builds the chunk list from the device cu_seqlens;
-//   chunk_intra_kernel   one CTA per (chunk, head): everything that does not depend on S0
+//   intra-chunk kernel   one CTA per (chunk, head): everything that does not depend on S0
 //                        (W, U, Q o e^G, K o e^{G_L-G}, P, e^{G_L}) into the workspace;
-//   chunk_state_kernel   one CTA per (sequence, head, value tile): the serial pass over the
-//                        sequence's chunks, keeping its slice of S on chip.
+//   state-pass kernel    the serial pass over a sequence's chunks, keeping S on chip.
+// bf16 inputs at C = 64, D = 128 take the tensor-core pair (chunk_intra_tc_kernel, two CTAs per SM,
+// and chunk_state_tc_kernel, one CTA per (sequence, head)), which exchange a per-(chunk, head)
+// record laid out as the state pass's shared-memory operand images (TcRec).  Every other shape and
+// fp32 inputs take the fp32 CUDA-core pair (chunk_intra_kernel; chunk_state_kernel with one CTA
+// per (sequence, head, value tile)), which meets the 1e-5 bound of fp32 I/O.
 //
 // Overflow-free decay algebra.  With these gates g reaches tens per token, so e^{-G} overflows
 // fp32 long before a chunk ends.  No decay factor here is ever formed from an exponent > 0:
