@@ -189,10 +189,14 @@ recurrent_kernel(const RecArgs a)
         s_sc[8 * t + 2] = alpha_h;
     }
     __syncthreads();
-    for (int t = warp; t < T; t += NWARPS) {             // one warp per token
+    // Norms and q.k.  Verify (T tokens): one warp per token, scaled k_hat and q_hat back to shared
+    // memory.  Decode and replay (one token): every warp reduces the token's norms itself and keeps
+    // 1/|k|, scale/|q| and q_hat.k_hat in registers, which saves two barriers.
+    float rk1 = 1.f, rq1 = 1.f, qk1 = 0.f;
+    if (MODE != kModeVerify) {
         float kk = 0.f, qq = 0.f, kq = 0.f;
         for (int c = lane; c < D; c += 32) {
-            const float kc = s_k[t * D + c], qc = s_q[t * D + c];
+            const float kc = s_k[c], qc = s_q[c];
             kk = fmaf(kc, kc, kk);
             qq = fmaf(qc, qc, qq);
             kq = fmaf(kc, qc, kq);
@@ -203,19 +207,38 @@ recurrent_kernel(const RecArgs a)
             qq += __shfl_xor_sync(0xffffffffu, qq, off);
             kq += __shfl_xor_sync(0xffffffffu, kq, off);
         }
-        if (lane == 0) {
-            const float rk = 1.0f / sqrtf(kk + a.gp.l2_eps);
-            const float rq = a.gp.scale / sqrtf(qq + a.gp.l2_eps);
-            s_sc[8 * t + 1] = kq * rk * rq;
-            s_sc[8 * t + 3] = rk;
-            s_sc[8 * t + 4] = rq;
+        rk1 = 1.0f / sqrtf(kk + a.gp.l2_eps);
+        rq1 = a.gp.scale / sqrtf(qq + a.gp.l2_eps);
+        qk1 = kq * rk1 * rq1;
+    } else {
+        for (int t = warp; t < T; t += NWARPS) {         // one warp per token
+            float kk = 0.f, qq = 0.f, kq = 0.f;
+            for (int c = lane; c < D; c += 32) {
+                const float kc = s_k[t * D + c], qc = s_q[t * D + c];
+                kk = fmaf(kc, kc, kk);
+                qq = fmaf(qc, qc, qq);
+                kq = fmaf(kc, qc, kq);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                kk += __shfl_xor_sync(0xffffffffu, kk, off);
+                qq += __shfl_xor_sync(0xffffffffu, qq, off);
+                kq += __shfl_xor_sync(0xffffffffu, kq, off);
+            }
+            if (lane == 0) {
+                const float rk = 1.0f / sqrtf(kk + a.gp.l2_eps);
+                const float rq = a.gp.scale / sqrtf(qq + a.gp.l2_eps);
+                s_sc[8 * t + 1] = kq * rk * rq;
+                s_sc[8 * t + 3] = rk;
+                s_sc[8 * t + 4] = rq;
+            }
         }
-    }
-    __syncthreads();
-    for (int e = tid; e < T * D; e += Sh::THREADS) {
-        const int t = e / D;
-        s_k[e] *= s_sc[8 * t + 3];
-        s_q[e] *= s_sc[8 * t + 4];
+        __syncthreads();
+        for (int e = tid; e < T * D; e += Sh::THREADS) {
+            const int t = e / D;
+            s_k[e] *= s_sc[8 * t + 3];
+            s_q[e] *= s_sc[8 * t + 4];
+        }
     }
     if (MODE == kModeReplay && wp > 0) {
         // S = Diag(prod_j a_j) S0 + sum_j d_j^T (k_j o prod_{i>j} a_i) over the wp committed steps
@@ -257,9 +280,9 @@ recurrent_kernel(const RecArgs a)
                     ck += __shfl_xor_sync(0xffffffffu, ck, off);
                     cq += __shfl_xor_sync(0xffffffffu, cq, off);
                 }
-                if (lane == 0) {
-                    s_ck[j] = ck;
-                    s_cq[j] = cq;
+                if (lane == 0) {                     // raw k, q in shared memory: apply the norms
+                    s_ck[j] = ck * rk1;
+                    s_cq[j] = cq * rq1;
                 }
             }
         } else {
@@ -287,15 +310,18 @@ recurrent_kernel(const RecArgs a)
                 }
         }
         }
+        __syncthreads();
     }
-    __syncthreads();
+    if (MODE == kModeVerify) __syncthreads();
 
     for (int t = 0; t < T; ++t) {
         const int64_t tok = b * T + t;
         const size_t rowbase = ((size_t)tok * H + h) * D;
         const float beta = s_sc[8 * t + 0];
-        const float qk = s_sc[8 * t + 1];
+        const float qk = MODE == kModeVerify ? s_sc[8 * t + 1] : qk1;
         const float alpha_h = s_sc[8 * t + 2];
+        const float sk = MODE == kModeVerify ? 1.f : rk1;   // k_hat = k * sk, q_hat = q * sq
+        const float sq = MODE == kModeVerify ? 1.f : rq1;
 
         // ---- per-lane column constants --------------------------------------------------------
         float kh[CPL], qh[CPL], al[CPL];
@@ -304,8 +330,13 @@ recurrent_kernel(const RecArgs a)
             const int c = t * D + 4 * (li + LPR * j);
             const float4 k4 = *reinterpret_cast<const float4*>(&s_k[c]);
             const float4 q4 = *reinterpret_cast<const float4*>(&s_q[c]);
-            kh[4 * j + 0] = k4.x; kh[4 * j + 1] = k4.y; kh[4 * j + 2] = k4.z; kh[4 * j + 3] = k4.w;
-            qh[4 * j + 0] = q4.x; qh[4 * j + 1] = q4.y; qh[4 * j + 2] = q4.z; qh[4 * j + 3] = q4.w;
+            if (MODE == kModeVerify) {
+                kh[4 * j + 0] = k4.x; kh[4 * j + 1] = k4.y; kh[4 * j + 2] = k4.z; kh[4 * j + 3] = k4.w;
+                qh[4 * j + 0] = q4.x; qh[4 * j + 1] = q4.y; qh[4 * j + 2] = q4.z; qh[4 * j + 3] = q4.w;
+            } else {
+                kh[4 * j + 0] = k4.x * sk; kh[4 * j + 1] = k4.y * sk; kh[4 * j + 2] = k4.z * sk; kh[4 * j + 3] = k4.w * sk;
+                qh[4 * j + 0] = q4.x * sq; qh[4 * j + 1] = q4.y * sq; qh[4 * j + 2] = q4.z * sq; qh[4 * j + 3] = q4.w * sq;
+            }
             if (GATE == KDA_GATE_PER_CHANNEL) {
                 const float4 a4 = *reinterpret_cast<const float4*>(&s_al[c]);
                 al[4 * j + 0] = a4.x; al[4 * j + 1] = a4.y; al[4 * j + 2] = a4.z; al[4 * j + 3] = a4.w;
@@ -389,7 +420,7 @@ recurrent_kernel(const RecArgs a)
         if (MODE == kModeReplay && !flush) {          // append k_hat and the decay of this step
             const size_t re = ((size_t)slot * H + h) * a.ring_len + wp;
             for (int c = tid; c < D; c += Sh::THREADS) {
-                a.ring_k[re * D + c] = s_k[c];
+                a.ring_k[re * D + c] = s_k[c] * rk1;
                 if (GATE == KDA_GATE_PER_CHANNEL) a.ring_a[re * D + c] = s_al[c];
             }
             if (GATE == KDA_GATE_PER_HEAD && tid == 0) a.ring_a[re] = alpha_h;
