@@ -90,6 +90,20 @@ WsLayout ws_layout(int C, int D, int H, int32_t N, int64_t T)
 // seq_order lists the sequences by decreasing chunk count (ties by index; identity when
 // N > 4096), so that the state pass starts its longest serial chains first.
 constexpr int32_t kMaxSortedSeqs = 4096;
+// token range of sequence i, clamped into [0, T] (a malformed cu_seqlens is recorded, not trusted)
+__device__ __forceinline__ void seq_range(const int32_t* __restrict__ cu, int32_t i, int32_t N, int64_t T,
+                                          int64_t& s0, int64_t& s1, bool record)
+{
+    s0 = cu[i];
+    s1 = cu[i + 1];
+    const bool bad = s0 < 0 || s1 < s0 || s1 > T || (i == 0 && s0 != 0) || (i == N - 1 && s1 != T);
+    if (bad) {
+        if (record) record_error(kDevErrSeqlens);
+        s0 = s0 < 0 ? 0 : (s0 > T ? T : s0);
+        s1 = s1 < s0 ? s0 : (s1 > T ? T : s1);
+    }
+}
+
 __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* __restrict__ cu, int32_t N, int64_t T,
                                                            int C, int64_t max_chunks,
                                                            int32_t* chunk_seq, int32_t* chunk_start,
@@ -101,19 +115,13 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* __rest
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) s_base = 0;
     __syncthreads();
+    // 1. chunk counts and their exclusive prefix sum -> seq_off
     for (int32_t base = 0; base < N; base += blockDim.x) {
         const int32_t i = base + tid;
-        int64_t s0 = 0, s1 = 0;
         int32_t n = 0;
         if (i < N) {
-            s0 = cu[i];
-            s1 = cu[i + 1];
-            const bool bad = s0 < 0 || s1 < s0 || s1 > T || (i == 0 && s0 != 0) || (i == N - 1 && s1 != T);
-            if (bad) {
-                record_error(kDevErrSeqlens);
-                s0 = s0 < 0 ? 0 : (s0 > T ? T : s0);
-                s1 = s1 < s0 ? s0 : (s1 > T ? T : s1);
-            }
+            int64_t s0, s1;
+            seq_range(cu, i, N, T, s0, s1, true);
             n = (int32_t)((s1 - s0 + C - 1) / C);
         }
         // inclusive scan of n over the CTA
@@ -137,26 +145,33 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* __rest
         __syncthreads();
         const int32_t incl = x + (warp > 0 ? s_warp[warp - 1] : 0);
         const int32_t off0 = s_base + incl - n;
-        if (i < N) {
-            seq_off[i] = off0;
-            for (int32_t m = 0; m < n; ++m) {
-                const int64_t c = (int64_t)off0 + m;
-                if (c >= max_chunks) {
-                    record_error(kDevErrSeqlens);
-                    break;
-                }
-                const int64_t st = s0 + (int64_t)m * C;
-                chunk_seq[c] = i;
-                chunk_start[c] = (int32_t)st;
-                chunk_len[c] = (int32_t)((s1 - st) < C ? (s1 - st) : C);
-            }
-        }
+        if (i < N) seq_off[i] = off0;
         __syncthreads();
         if (tid == blockDim.x - 1) s_base = off0 + n;
         __syncthreads();
     }
-    if (tid == 0) seq_off[N] = s_base;
+    if (tid == 0) {
+        seq_off[N] = s_base;
+        if (s_base > max_chunks) record_error(kDevErrSeqlens);
+    }
     __syncthreads();
+    // 2. one thread per chunk: its sequence by binary search over seq_off, then start and length
+    const int64_t nch = s_base < max_chunks ? s_base : max_chunks;
+    for (int64_t c = tid; c < nch; c += blockDim.x) {
+        int32_t lo = 0, hi = N - 1;                  // last i with seq_off[i] <= c
+        while (lo < hi) {
+            const int32_t mid = (lo + hi + 1) >> 1;
+            if (seq_off[mid] <= c) lo = mid;
+            else hi = mid - 1;
+        }
+        int64_t s0, s1;
+        seq_range(cu, lo, N, T, s0, s1, false);
+        const int64_t st = s0 + (c - seq_off[lo]) * C;
+        chunk_seq[c] = lo;
+        chunk_start[c] = (int32_t)st;
+        chunk_len[c] = (int32_t)((s1 - st) < C ? (s1 - st) : C);
+    }
+    // 3. sequences by decreasing chunk count
     for (int32_t i = tid; i < N; i += blockDim.x) {
         if (N > kMaxSortedSeqs) {
             seq_order[i] = i;
