@@ -19,9 +19,9 @@ def _step_rows(inp, B, steps, t):
     return {n: inp[n][rows].contiguous().to(DEV) for n in ("q", "k", "v", "g_raw", "b_raw")}
 
 
-@pytest.mark.parametrize("gate", ["kda", "gdn"])
-def test_ring_length_one_is_plain_decode(gate):
-    H, D, B, steps = 4, 128, 6, 5
+@pytest.mark.parametrize("gate,D", [("kda", 128), ("gdn", 128), ("kda", 32), ("gdn", 64)])
+def test_ring_length_one_is_plain_decode(gate, D):
+    H, B, steps = 4, 6, 5
     inp = workloads.make_inputs([steps] * B, H, D, torch.float32, gate=gate, pool_slots=8, pool_std=0.2, seed=81)
     d = workloads.to_device(inp, DEV)
     pool_a, pool_b = d["pool"].clone(), d["pool"].clone()
@@ -38,9 +38,12 @@ def test_ring_length_one_is_plain_decode(gate):
         assert torch.equal(pool_a, pool_b)
 
 
-@pytest.mark.parametrize("gate,io,L", [("kda", torch.bfloat16, 8), ("kda", torch.float32, 16), ("gdn", torch.bfloat16, 4)])
-def test_replay_matches_oracle_over_many_steps(gate, io, L):
-    H, D, B, steps = 4, 128, 7, 21
+@pytest.mark.parametrize("gate,io,L,D", [("kda", torch.bfloat16, 8, 128), ("kda", torch.float32, 16, 128),
+                                          ("gdn", torch.bfloat16, 4, 128), ("kda", torch.float32, 8, 16),
+                                          ("gdn", torch.bfloat16, 8, 32), ("kda", torch.float32, 5, 64),
+                                          ("kda", torch.bfloat16, 32, 128)])
+def test_replay_matches_oracle_over_many_steps(gate, io, L, D):
+    H, B, steps = 4, 7, 21
     inp = workloads.make_inputs([steps] * B, H, D, io, gate=gate, pool_slots=10, pool_std=0.05, seed=82,
                                 dt_bias_std=0.3, padding_rows=(5,))
     o_ref, p_ref, _ = oracle_run(inp, H, D, gate=gate)             # token-by-token over each request
