@@ -1499,10 +1499,15 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
 #pragma unroll
     for (int i = 0; i < 6; ++i)
         *reinterpret_cast<uint4*>(sIB + 16 * (tid + THREADS * i)) = make_uint4(bimg[i][0], bimg[i][1], bimg[i][2], bimg[i][3]);
-    for (int e = tid; e < C * LDA; e += THREADS) {            // A <- diagonal blocks; T <- 0
-        const int r = e / LDA, jj = e - r * LDA;
-        sA[e] = (jj < C && (r >> 4) == (jj >> 4)) ? sAD[r * 16 + (jj & 15)] : 0.f;
-        sT[e] = 0.f;
+    {                                                         // A <- diagonal blocks; T <- 0
+        const int r = tid >> 2, q = tid & 3;                  // row r, float4 groups q, q + 4, ..
+        const int b4 = (r >> 4) * 4;                          // the row's diagonal block: groups b4 .. b4 + 3
+        for (int f = q; f < LDA / 4; f += 4) {
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (f >= b4 && f < b4 + 4) x = ld4(sAD + r * 16 + 4 * (f - b4));
+            st4(sA + r * LDA + 4 * f, x);
+            st4(sT + r * LDA + 4 * f, make_float4(0.f, 0.f, 0.f, 0.f));
+        }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc::tc_fence_before();
