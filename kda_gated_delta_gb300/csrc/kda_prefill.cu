@@ -1532,7 +1532,13 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
     for (int hh = 0; hh < 2; ++hh) {
         float x[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = tc::round_tf32(sBeta[32 * jh + 16 * hh + i] * vr[16 * hh + i]);
+        for (int i4 = 0; i4 < 4; ++i4) {
+            const float4 b4 = ld4(sBeta + 32 * jh + 16 * hh + 4 * i4);
+            x[4 * i4 + 0] = tc::round_tf32(b4.x * vr[16 * hh + 4 * i4 + 0]);
+            x[4 * i4 + 1] = tc::round_tf32(b4.y * vr[16 * hh + 4 * i4 + 1]);
+            x[4 * i4 + 2] = tc::round_tf32(b4.z * vr[16 * hh + 4 * i4 + 2]);
+            x[4 * i4 + 3] = tc::round_tf32(b4.w * vr[16 * hh + 4 * i4 + 3]);
+        }
         tc::tmem_st16_nowait(tmem + lane_base + T_KD + 32 * jh + 16 * hh, x);
     }
     if ((warp & 3) < 3) {          // Gram rows m = (I, j): warp half 0 -> A (k rows), half 1 -> P (q rows)
@@ -1582,7 +1588,13 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
             const float* tc0 = sT + 16 * J * LDA + 16 * J + jj;
             float acc = 0.f;
 #pragma unroll
-            for (int kk = 0; kk < 16 * d; ++kk) acc = fmaf(ar[kk], tc0[kk * LDA], acc);
+            for (int kk = 0; kk < 16 * d; kk += 4) {                // a row of A as float4s
+                const float4 av = ld4(ar + kk);
+                acc = fmaf(av.x, tc0[kk * LDA], acc);
+                acc = fmaf(av.y, tc0[(kk + 1) * LDA], acc);
+                acc = fmaf(av.z, tc0[(kk + 2) * LDA], acc);
+                acc = fmaf(av.w, tc0[(kk + 3) * LDA], acc);
+            }
             sX[e] = acc;
         }
         __syncthreads();
@@ -1592,7 +1604,13 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
             const float* xc = sX + (J << 8) + jj;
             float acc = 0.f;
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk) acc = kk <= i ? fmaf(tr[kk], xc[kk * 16], acc) : acc;
+            for (int kk = 0; kk < 16; kk += 4) {                    // T_II is lower triangular
+                const float4 tv = ld4(tr + kk);
+                acc = kk + 0 <= i ? fmaf(tv.x, xc[kk * 16], acc) : acc;
+                acc = kk + 1 <= i ? fmaf(tv.y, xc[(kk + 1) * 16], acc) : acc;
+                acc = kk + 2 <= i ? fmaf(tv.z, xc[(kk + 2) * 16], acc) : acc;
+                acc = kk + 3 <= i ? fmaf(tv.w, xc[(kk + 3) * 16], acc) : acc;
+            }
             sT[(16 * I + i) * LDA + 16 * J + jj] = -acc;
         }
         __syncthreads();
