@@ -1158,8 +1158,8 @@ constexpr uint32_t OFF_BP = OFF_AD + NB * 256 * 4;   // block products bp      [
 constexpr uint32_t OFF_EB = OFF_BP + NB * D * 4;     // e^{G} before block b: prod_{b' < b} bp  [NB][D]
 constexpr uint32_t OFF_B12 = OFF_EB + NB * D * 4;    // bp[1] * bp[2]          [D]
 constexpr uint32_t OFF_BETA = OFF_B12 + D * 4;       // beta                   [C]
-constexpr uint32_t OFF_BAR = OFF_BETA + C * 4;       // 2 mbarriers
-constexpr uint32_t OFF_TM = OFF_BAR + 16;            // TMEM base
+constexpr uint32_t OFF_BAR = OFF_BETA + C * 4;       // 3 mbarriers: Gram done, U/W done, drain
+constexpr uint32_t OFF_TM = OFF_BAR + 24;            // TMEM base
 constexpr uint32_t BYTES = OFF_TM + 16;
 constexpr uint32_t OFF_A = OFF_K;                    // A = sum of diagonal and Gram blocks [C][LDA]
 constexpr uint32_t OFF_X = OFF_K + C * LDA * 4;      // 3 scratch 16 x 16 blocks
@@ -1196,6 +1196,7 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
     unsigned char* sIB = sm + OFF_IB;
     uint64_t* bar_g = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     uint64_t* bar_uw = bar_g + 1;
+    uint64_t* bar_drain = bar_g + 2;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + OFF_TM);
 
     const int64_t ch = blockIdx.x;
@@ -1211,6 +1212,7 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
     const int L = a.chunk_len[ch];
     const int H = a.H;
     const float rate = expf(a.A_log[h]);
+    bool tc_ok = true;                                       // thread 0: every tcgen05 wait completed
     const __nv_bfloat16* kp = reinterpret_cast<const __nv_bfloat16*>(a.k);
     const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(a.q);
     const __nv_bfloat16* vp = reinterpret_cast<const __nv_bfloat16*>(a.v);
@@ -1226,6 +1228,7 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
     if (tid == 0) {
         tc::mbar_init(bar_g, 1);
         tc::mbar_init(bar_uw, 1);
+        tc::mbar_init(bar_drain, 1);
         tc::fence_mbar_init();
     }
     if (warp == 1) {               // the value rows are read after the Gram: start them towards L2 now
@@ -1527,6 +1530,7 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
         const bool done = tc::mbar_wait(bar_g, 0, kWaitPolls);
         tc::tc_fence_after();
         if (!done && tid == 0) record_error(kDevErrTimeout);
+        if (tid == 0) tc_ok = tc_ok && done;
     }
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
@@ -1642,6 +1646,7 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
     {
         const bool done = tc::mbar_wait(bar_uw, 0, kWaitPolls);
         tc::tc_fence_after();
+        if (tid == 0) tc_ok = tc_ok && done;
         if (!done) {
             if (lane == 0) record_error(kDevErrTimeout);
         } else {
@@ -1660,6 +1665,10 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
                 }
             }
         }
+    }
+    if (tid == 0 && !tc_ok) {      // a wait gave up: let this CTA's MMAs land (bounded) before freeing TMEM
+        tc::mma_commit(bar_drain);
+        tc::mbar_wait(bar_drain, 0, kWaitPolls);
     }
     tc::tc_fence_before();
     __syncthreads();
