@@ -58,7 +58,7 @@ typedef enum kda_status {
     KDA_ERR_MISALIGNED = -3,   /* a tensor pointer is not 16-byte aligned */
     KDA_ERR_WORKSPACE = -4,    /* workspace NULL, too small or not 256-byte aligned */
     KDA_ERR_CUDA = -5,         /* a CUDA runtime call or kernel launch failed */
-    KDA_ERR_DEVICE_CHECK = -6, /* kda_check_device_errors found a recorded argument error */
+    KDA_ERR_DEVICE_CHECK = -6, /* kda_check_device_errors found an error a kernel recorded */
     KDA_ERR_SCRATCH_LIMIT = -7 /* the problem needs more scratch than KDA_STATIC_SCRATCH_BYTES */
 } kda_status;
 
@@ -287,6 +287,22 @@ int32_t kda_chunk_prefill_static_scratch(const kda_params* p,
  * recorded, KDA_ERR_DEVICE_CHECK when one was, KDA_ERR_CUDA when the synchronisation failed.
  */
 int32_t kda_check_device_errors(kda_stream_t stream, int32_t* code);
+
+/*
+ * Failure-detection self-test of the bounded waits in the tensor-core kernels.  Enqueues one
+ * warp on `stream` that allocates 32 TMEM columns, waits with a limit of `polls` polls on an
+ * mbarrier that nothing arrives on, records device error 3 (timeout) when the wait gives up,
+ * then takes the same exit path as the prefill kernels after a timeout: commit to a second
+ * mbarrier and wait for it (again at most `polls` polls), free TMEM, return.  No fault, trap or
+ * unbounded loop is involved, and the context stays usable.
+ *   polls   in [1, 1 << 24]; one poll is one mbarrier try_wait.
+ *   result  NULL, or caller-owned device int32[2]: result[0] = 1 if the first wait completed
+ *           (it never should), result[1] = 1 if the drain completed.  Written by the kernel.
+ * Returns KDA_OK when the kernel was enqueued, KDA_ERR_INVALID_ARG for polls outside the range,
+ * KDA_ERR_MISALIGNED when result is not 4-byte aligned, KDA_ERR_CUDA when the launch failed.
+ * kda_check_device_errors then reports code 3.
+ */
+int32_t kda_selftest_wait_timeout(uint32_t polls, int32_t* result, kda_stream_t stream);
 
 #ifdef __cplusplus
 }

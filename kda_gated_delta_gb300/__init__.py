@@ -16,5 +16,6 @@ from .binding import (  # noqa: F401
     recurrent_verify,
     replay_decode,
     replay_rings,
+    selftest_wait_timeout,
     status_string,
 )

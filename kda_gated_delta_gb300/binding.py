@@ -95,6 +95,8 @@ def lib() -> ctypes.CDLL:
                                                  _P, ctypes.c_int64, _P, _P]
         L.kda_check_device_errors.restype = ctypes.c_int32
         L.kda_check_device_errors.argtypes = [_P, ctypes.POINTER(ctypes.c_int32)]
+        L.kda_selftest_wait_timeout.restype = ctypes.c_int32
+        L.kda_selftest_wait_timeout.argtypes = [ctypes.c_uint32, _P, _P]
         _lib = L
         return L
 
@@ -322,6 +324,20 @@ def commit_verified_states(inter, accept_len, state_pool, state_idx, *, params: 
                                           _ptr(state_pool), state_pool.shape[0], _ptr(state_idx), _stream(stream))
     _check(rc, "kda_commit_verified_states")
     return state_pool
+
+
+def selftest_wait_timeout(polls: int, result=None, stream=None) -> None:
+    """Enqueue the bounded-wait self-test (a wait that cannot complete; see kda.h).
+
+    result: None or a device int32 tensor of 2 elements that receives (first wait completed,
+    drain completed).  The timeout is then reported by check_device_errors() as code 3."""
+    if result is not None:
+        _dev(result, "result", torch.int32)
+        if result.numel() < 2:
+            raise ValueError("result must hold 2 int32 elements")
+    rc = lib().kda_selftest_wait_timeout(int(polls), _ptr(result) if result is not None else None,
+                                         _stream(stream))
+    _check(rc, "kda_selftest_wait_timeout")
 
 
 def check_device_errors(stream=None) -> int:

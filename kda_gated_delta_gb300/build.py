@@ -17,7 +17,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libkda.so")
 
-SOURCES = ["kda_api.cu", "kda_recurrent.cu", "kda_prefill.cu", "kda_prefill_static.cu"]
+SOURCES = ["kda_api.cu", "kda_recurrent.cu", "kda_prefill.cu", "kda_prefill_static.cu",
+           "kda_selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -72,7 +72,7 @@ const char* kda_status_string(int32_t status)
     case KDA_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
     case KDA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
     case KDA_ERR_CUDA: return "CUDA runtime error";
-    case KDA_ERR_DEVICE_CHECK: return "a kernel recorded an invalid state_idx or cu_seqlens";
+    case KDA_ERR_DEVICE_CHECK: return "a kernel recorded an error (bad state_idx, cu_seqlens, accept_len or write_pos, or a bounded wait that gave up)";
     case KDA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the library's fixed scratch array holds";
     default: return "unknown status";
     }
@@ -228,11 +228,19 @@ int32_t kda_check_device_errors(kda_stream_t stream, int32_t* code)
     if (!code) return KDA_ERR_INVALID_ARG;
     *code = 0;
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return KDA_ERR_CUDA;
-    int32_t c1 = 0, c2 = 0;
+    int32_t c1 = 0, c2 = 0, c3 = 0;
     if (kda::recurrent_read_and_clear_error(&c1) != cudaSuccess) return KDA_ERR_CUDA;
     if (kda::prefill_read_and_clear_error(&c2) != cudaSuccess) return KDA_ERR_CUDA;
-    *code = c1 ? c1 : c2;
+    if (kda::selftest_read_and_clear_error(&c3) != cudaSuccess) return KDA_ERR_CUDA;
+    *code = c1 ? c1 : (c2 ? c2 : c3);
     return *code ? KDA_ERR_DEVICE_CHECK : KDA_OK;
+}
+
+int32_t kda_selftest_wait_timeout(uint32_t polls, int32_t* result, kda_stream_t stream)
+{
+    if (polls < 1u || polls > (1u << 24)) return KDA_ERR_INVALID_ARG;
+    if (result && (reinterpret_cast<uintptr_t>(result) & 3u)) return KDA_ERR_MISALIGNED;
+    return from_cuda(kda::launch_wait_selftest(polls, result, (cudaStream_t)stream));
 }
 
 }  // extern "C"

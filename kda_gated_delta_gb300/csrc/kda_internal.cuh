@@ -88,5 +88,7 @@ cudaError_t launch_prefill(const kda_params& p, const GateParams& gp, const void
                            float* chunk_states = nullptr, int64_t chunk_states_capacity = 0);
 bool prefill_supported(const kda_params& p);
 cudaError_t prefill_read_and_clear_error(int32_t* code);
+cudaError_t launch_wait_selftest(uint32_t polls, int32_t* result, cudaStream_t stream);
+cudaError_t selftest_read_and_clear_error(int32_t* code);
 
 }  // namespace kda

@@ -116,3 +116,13 @@ def test_prefill_validation_and_workspace(L):
     assert call(p, cu=None) == -1
     assert call(p, T=0) == 0 and call(p, N=0) == 0
     assert call(p, N=-1) == -1
+
+
+def test_selftest_validation(L):
+    """The bounded-wait self-test checks its arguments on the host before any CUDA call."""
+    f = L.kda_selftest_wait_timeout
+    f.restype = ctypes.c_int32
+    f.argtypes = [ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p]
+    assert f(0, None, None) == -1
+    assert f((1 << 24) + 1, None, None) == -1
+    assert f(8, FAKE + 2, None) == -3
