@@ -1237,13 +1237,16 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
                          : "memory");
     }
     // 1. loads, all issued before any is used (rows past the chunk end: k = q = 0, alpha = 1,
-    //    beta = 0).  k, q: 8 elements in rows (tid >> 4) + 16 i; g: 4 elements in rows (tid >> 5) + 8 i
+    //    beta = 0).  k, q: 8 elements in rows 2 warp + (lane bit 2) + 16 i, columns 32 (lane >> 3) +
+    //    8 (lane & 3): the two 8-lane halves of a quarter-warp hold adjacent rows, so that with the
+    //    132-float row stride each 16-byte shared store of a quarter-warp covers all 32 banks once.
+    //    g: 4 elements in rows (tid >> 5) + 8 i
     {
         uint4 kv[4], qv[4];
         float4 gv[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int r = (tid >> 4) + 16 * i, c8 = (tid & 15) * 8;
+            const int r = 2 * warp + ((lane >> 2) & 1) + 16 * i, c8 = 32 * (lane >> 3) + 8 * (lane & 3);
             kv[i] = qv[i] = make_uint4(0, 0, 0, 0);
             if (r < L) {
                 const size_t idx = ((size_t)(t0 + r) * H + h) * D + c8;
@@ -1264,8 +1267,8 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
         if (a.dt_bias) db = *reinterpret_cast<const float4*>(a.dt_bias + (size_t)h * D + c4);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            // the 16 consecutive lanes that hold row r reduce its squared norms with shuffles
-            const int r = (tid >> 4) + 16 * i, c8 = (tid & 15) * 8;
+            // the 16 lanes that hold row r (lane bit 2 fixed) reduce its squared norms with shuffles
+            const int r = 2 * warp + ((lane >> 2) & 1) + 16 * i, c8 = 32 * (lane >> 3) + 8 * (lane & 3);
             const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&kv[i]);
             const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(&qv[i]);
             float kf[8], qf[8], kk = 0.f, qq = 0.f;
@@ -1277,7 +1280,8 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
                 qq = fmaf(qf[t], qf[t], qq);
             }
 #pragma unroll
-            for (int off = 8; off > 0; off >>= 1) {
+            for (int off = 1; off <= 16; off <<= 1) {
+                if (off == 4) continue;
                 kk += __shfl_xor_sync(0xffffffffu, kk, off);
                 qq += __shfl_xor_sync(0xffffffffu, qq, off);
             }
@@ -1448,13 +1452,14 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
     __syncthreads();
 
     // value loads for (beta V)^T (lane v, columns j = 32 jh ..), issued here so that their latency
-    // overlaps the Gram operands; consumed after the Gram completes
+    // overlaps the Gram operands; consumed after the Gram completes.  They stay raw bf16 bits until
+    // then: converting at the load would make the thread wait for the data here.
     const int vv_ = tid & (D - 1), jh = tid >> 7;
-    float vr[32];
+    unsigned short vr[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         const int j = 32 * jh + i;
-        vr[i] = j < L ? __bfloat162float(vp[((size_t)(t0 + j) * H + h) * D + vv_]) : 0.f;
+        vr[i] = j < L ? __bfloat16_as_ushort(vp[((size_t)(t0 + j) * H + h) * D + vv_]) : (unsigned short)0;
     }
 
     // 4. Gram operands and the Qbar record.  B image chunk f (16 bytes = 8 fp16 of one row) sits at
@@ -1538,10 +1543,12 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
 #pragma unroll
         for (int i4 = 0; i4 < 4; ++i4) {
             const float4 b4 = ld4(sBeta + 32 * jh + 16 * hh + 4 * i4);
-            x[4 * i4 + 0] = tc::round_tf32(b4.x * vr[16 * hh + 4 * i4 + 0]);
-            x[4 * i4 + 1] = tc::round_tf32(b4.y * vr[16 * hh + 4 * i4 + 1]);
-            x[4 * i4 + 2] = tc::round_tf32(b4.z * vr[16 * hh + 4 * i4 + 2]);
-            x[4 * i4 + 3] = tc::round_tf32(b4.w * vr[16 * hh + 4 * i4 + 3]);
+#define KDA_VF(i) __bfloat162float(__ushort_as_bfloat16(vr[i]))
+            x[4 * i4 + 0] = tc::round_tf32(b4.x * KDA_VF(16 * hh + 4 * i4 + 0));
+            x[4 * i4 + 1] = tc::round_tf32(b4.y * KDA_VF(16 * hh + 4 * i4 + 1));
+            x[4 * i4 + 2] = tc::round_tf32(b4.z * KDA_VF(16 * hh + 4 * i4 + 2));
+            x[4 * i4 + 3] = tc::round_tf32(b4.w * KDA_VF(16 * hh + 4 * i4 + 3));
+#undef KDA_VF
         }
         tc::tmem_st16_nowait(tmem + lane_base + T_KD + 32 * jh + 16 * hh, x);
     }
