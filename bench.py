@@ -37,10 +37,10 @@ UNIT = "tokens/s"
 # step, caches flushed before each kernel), valid only for the kernel source they were taken on.
 MEASURED_TRAFFIC = {
     "kda_prefill.cu": {"sha256_16": "c45683e980ef8a5c",
-                       "kda_chunk_table": 0.0, "kda_chunk_intra": 1869.8e6, "kda_chunk_state": 1393.4e6},
-    "kda_recurrent.cu": {"sha256_16": "3bfc315eee160f07",
-                         "kda_recurrent_decode": 1024.8e6, "kda_recurrent_verify": 614.3e6,
-                         "kda_replay_decode": 620.3e6},
+                       "kda_chunk_table": 0.0, "kda_chunk_intra": 1869.7e6, "kda_chunk_state": 1393.3e6},
+    "kda_recurrent.cu": {"sha256_16": "302ea2e2dab4d254",
+                         "kda_recurrent_decode": 1024.6e6, "kda_recurrent_verify": 614.1e6,
+                         "kda_replay_decode": 620.5e6},
 }
 
 

@@ -132,16 +132,6 @@ recurrent_kernel(const RecArgs a)
     const int li = lane % LPR;
     const size_t tile = ((size_t)slot * H + h) * (size_t)D * D;
 
-    // Issue every state load of this thread first; the token prologue overlaps their latency.
-    float4 st[STEPS][NV4];
-#pragma unroll
-    for (int s = 0; s < STEPS; ++s) {
-        const int row = warp * Sh::ROWS_PER_WARP + s * RPS + row_in_step;
-        const float4* src = reinterpret_cast<const float4*>(a.pool_in + tile + (size_t)row * D);
-#pragma unroll
-        for (int j = 0; j < NV4; ++j) st[s][j] = __ldcs(src + li + LPR * j);
-    }
-
     // ---- prologue for all T tokens at once: inputs to shared memory, then norms, q.k, beta, alpha
     extern __shared__ float4 rec_smem4[];
     float* s_k = reinterpret_cast<float*>(rec_smem4);    // [T][D] k -> k_hat
@@ -150,8 +140,8 @@ recurrent_kernel(const RecArgs a)
     float* s_v = s_al + T * D;                           // [T][D] v
     float* s_sc = s_v + T * D;                           // [T][8]: beta, q.k, alpha (per head), 1/|k|, scale/|q|
     if (MODE == kModeReplay && wp > 0) {
-        // the committed ring entries travel to shared memory (asynchronous 16-byte copies) while
-        // the state loads and the prologue proceed
+        // the committed ring entries travel to shared memory (asynchronous 16-byte copies), issued
+        // ahead of the state loads so that they land first
         float* s_rk = s_sc + 8 * T;
         float* s_rd = s_rk + a.ring_len * D;
         float* s_ra = s_rd + a.ring_len * D;
@@ -169,24 +159,71 @@ recurrent_kernel(const RecArgs a)
     const TIn* qp = reinterpret_cast<const TIn*>(a.q);
     const TIn* kp = reinterpret_cast<const TIn*>(a.k);
     const TIn* vp = reinterpret_cast<const TIn*>(a.v);
-    const float rate = expf(a.A_log[h]);
-    for (int e = tid; e < T * D; e += Sh::THREADS) {
-        const int t = e / D, c = e - t * D;
-        const size_t idx = ((size_t)(b * T + t) * H + h) * D + c;
-        s_k[e] = to_f32(kp[idx]);
-        s_q[e] = to_f32(qp[idx]);
-        s_v[e] = to_f32(vp[idx]);
-        if (GATE == KDA_GATE_PER_CHANNEL) {
-            const float x = a.g_raw[idx] + (a.dt_bias ? a.dt_bias[(size_t)h * D + c] : 0.f);
-            s_al[e] = expf(gate_log_decay(x, rate, a.gp));
+    // One token (decode, replay): its inputs are loaded raw before the state, so that they arrive
+    // first and the prologue's arithmetic overlaps the state's latency instead of following it.
+    TIn k_raw{}, q_raw{}, v_raw{};
+    float g_r = 0.f, dt_r = 0.f, b_r = 0.f;
+    if (!VERIFY) {
+        if (tid < D) {
+            const size_t idx = ((size_t)b * H + h) * D + tid;
+            k_raw = kp[idx];
+            q_raw = qp[idx];
+            v_raw = vp[idx];
+            if (GATE == KDA_GATE_PER_CHANNEL) {
+                g_r = a.g_raw[idx];
+                if (a.dt_bias) dt_r = a.dt_bias[(size_t)h * D + tid];
+            }
+        }
+        if (tid == 0) {
+            b_r = a.b_raw[(size_t)b * H + h];
+            if (GATE == KDA_GATE_PER_HEAD) {
+                g_r = a.g_raw[(size_t)b * H + h];
+                if (a.dt_bias) dt_r = a.dt_bias[h];
+            }
         }
     }
-    for (int t = tid; t < T; t += Sh::THREADS) {
-        const size_t th = (size_t)(b * T + t) * H + h;
-        s_sc[8 * t + 0] = sigmoid_f32(a.b_raw[th]);
-        float alpha_h = 1.f;
-        if (GATE == KDA_GATE_PER_HEAD) alpha_h = expf(gate_log_decay(a.g_raw[th] + (a.dt_bias ? a.dt_bias[h] : 0.f), rate, a.gp));
-        s_sc[8 * t + 2] = alpha_h;
+    const float a_log = a.A_log[h];
+    // Then every state load of this thread; the token prologue overlaps their latency.
+    float4 st[STEPS][NV4];
+#pragma unroll
+    for (int s = 0; s < STEPS; ++s) {
+        const int row = warp * Sh::ROWS_PER_WARP + s * RPS + row_in_step;
+        const float4* src = reinterpret_cast<const float4*>(a.pool_in + tile + (size_t)row * D);
+#pragma unroll
+        for (int j = 0; j < NV4; ++j) st[s][j] = __ldcs(src + li + LPR * j);
+    }
+
+    const float rate = expf(a_log);
+    if (VERIFY) {
+        for (int e = tid; e < T * D; e += Sh::THREADS) {
+            const int t = e / D, c = e - t * D;
+            const size_t idx = ((size_t)(b * T + t) * H + h) * D + c;
+            s_k[e] = to_f32(kp[idx]);
+            s_q[e] = to_f32(qp[idx]);
+            s_v[e] = to_f32(vp[idx]);
+            if (GATE == KDA_GATE_PER_CHANNEL) {
+                const float x = a.g_raw[idx] + (a.dt_bias ? a.dt_bias[(size_t)h * D + c] : 0.f);
+                s_al[e] = expf(gate_log_decay(x, rate, a.gp));
+            }
+        }
+        for (int t = tid; t < T; t += Sh::THREADS) {
+            const size_t th = (size_t)(b * T + t) * H + h;
+            s_sc[8 * t + 0] = sigmoid_f32(a.b_raw[th]);
+            float alpha_h = 1.f;
+            if (GATE == KDA_GATE_PER_HEAD) alpha_h = expf(gate_log_decay(a.g_raw[th] + (a.dt_bias ? a.dt_bias[h] : 0.f), rate, a.gp));
+            s_sc[8 * t + 2] = alpha_h;
+        }
+    } else {
+        if (tid < D) {
+            s_k[tid] = to_f32(k_raw);
+            s_q[tid] = to_f32(q_raw);
+            s_v[tid] = to_f32(v_raw);
+            if (GATE == KDA_GATE_PER_CHANNEL) s_al[tid] = expf(gate_log_decay(g_r + dt_r, rate, a.gp));
+        }
+        if (tid == 0) {
+            s_sc[0] = sigmoid_f32(b_r);
+            s_sc[2] = GATE == KDA_GATE_PER_HEAD ? expf(gate_log_decay(g_r + dt_r, rate, a.gp)) : 1.f;
+        }
     }
     __syncthreads();
     // Norms and q.k.  Verify (T tokens): one warp per token, scaled k_hat and q_hat back to shared
