@@ -66,3 +66,15 @@ def test_algorithmic_byte_counts():
     assert bench.prefill_bytes(0, 1, 1, 128, 2, 2) == 2 * 128 * 128 * 4 + 4 + 512
     # verify (per-head gate): one state read, per draft one state write and its token's bytes
     assert bench.verify_bytes(1, 4, 1, 128, 2, 2) == 65536 + 4 * (65536 + 768 + 4 + 4 + 256) + 8
+
+
+def test_per_kernel_algorithmic_bytes_partition_the_call():
+    """The intra kernel's bytes (token inputs once) and the state pass's (states read and written,
+    output written) add up to the prefill call's algorithmic bytes: the dominant-kernel roofline
+    neither double-counts nor drops a tensor."""
+    T, N, H, D = 16412, 8, 32, 128
+    for io, out in ((2, 2), (2, 4), (4, 4)):
+        call = bench.prefill_bytes(T, N, H, D, io, out)
+        assert bench.intra_bytes(T, H, D, io) + bench.state_pass_bytes(T, N, H, D, out) == call
+    # per (token, head): q, k, v bf16 + g_raw fp32 + b_raw fp32 = 1284 bytes
+    assert bench.intra_bytes(1, 1, 128, 2) - (4 + 128 * 4) == 1284
