@@ -126,3 +126,61 @@ def test_selftest_validation(L):
     assert f(0, None, None) == -1
     assert f((1 << 24) + 1, None, None) == -1
     assert f(8, FAKE + 2, None) == -3
+
+
+def test_replay_validation(L):
+    """kda_replay_decode: ring length in [1, 32], ring buffers and cursors present and aligned."""
+    f = L.kda_replay_decode
+
+    def call(p=None, batch=4, ring_len=8, rd=FAKE, rk=FAKE, ra=FAKE, wp=FAKE, out=FAKE):
+        p = _params() if p is None else p
+        return f(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, batch, FAKE, 8, FAKE,
+                 rd, rk, ra, ring_len, wp, None, out, None)
+
+    assert call(ring_len=0) == -1
+    assert call(ring_len=33) == -1
+    assert call(batch=-1) == -1
+    assert call(p=_params(D=48)) == -2
+    assert call(rd=None) == -1
+    assert call(wp=None) == -1
+    assert call(out=None) == -1
+    assert call(rk=MIS) == -3
+    assert call(ra=MIS) == -3
+    assert call(batch=0) == 0
+
+
+def test_commit_validation(L):
+    """kda_commit_verified_states: t_draft in [1, 16], buffers present, 16-byte aligned states."""
+    f = L.kda_commit_verified_states
+    p = _params()
+
+    def call(p=p, inter=FAKE, batch=4, t_draft=4, acc=FAKE, pool=FAKE):
+        return f(ctypes.byref(p) if p is not None else None, inter, batch, t_draft, acc, pool, 8, FAKE, None)
+
+    assert call(p=None) == -1
+    assert call(t_draft=0) == -1
+    assert call(t_draft=17) == -1
+    assert call(batch=-1) == -1
+    assert call(p=_params(D=48)) == -2
+    assert call(inter=None) == -1
+    assert call(acc=None) == -1
+    assert call(inter=MIS) == -3
+    assert call(pool=MIS) == -3
+    assert call(batch=0) == 0
+
+
+def test_snapshot_and_timed_prefill_validation(L):
+    """kda_chunk_prefill_snapshots needs an aligned snapshot buffer and a non-negative capacity;
+    kda_chunk_prefill_timed needs KDA_PREFILL_PHASE_EVENTS non-null event handles."""
+    p = _params(D=128, chunk_size=64)
+    wsb = binding.prefill_workspace_size(p, 2, 100)
+    args = (ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 2, 100, FAKE, 8, FAKE, FAKE,
+            FAKE, wsb)
+    snap = L.kda_chunk_prefill_snapshots
+    assert snap(*args, None, 10, None) == -1
+    assert snap(*args, FAKE, -1, None) == -1
+    assert snap(*args, MIS, 10, None) == -3
+    timed = L.kda_chunk_prefill_timed
+    assert timed(*args, None, None) == -1
+    events = (ctypes.c_void_p * 4)()                            # all null
+    assert timed(*args, None, events) == -1
