@@ -10,10 +10,17 @@ Every input lives in HBM before the timed region; each of the three working sets
 the 129 MB L2, so no L2 flush is needed between steps.  Kernel durations come from CUDA events
 recorded on the launching stream (the prefill's three kernels through kda_chunk_prefill_timed).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  * buffered (ReplaySSM) decode of the decode workload                       -> "decode_replay"
+Outside the timed steps, on rank 0: the tiny fp32 prefill's launch latency ("tiny", us per call)
+and the long prefill, 1 sequence of 131072 tokens as 32 successive 4096-token calls carrying
+the state ("long_prefill").
 
-Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle instead, on a
-bounded sample of the prefill workload, and prints the same metric.
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--only prefill]
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle instead, over the
+whole varlen workload per step, and prints the same metric.  ``--only prefill`` runs the varlen
+prefill alone (no decode, verify, tiny or long workloads, no e2e or CPU baseline): a small
+process for profiler captures.
 """
 from __future__ import annotations
 
@@ -208,29 +215,6 @@ def barrier(dist):
 _PREFILL_HOST = {}
 
 
-def oracle_prefill_sample(n_tokens):
-    """Oracle prefill of the first ``n_tokens`` tokens of the varlen workload's first sequence, all
-    32 heads, threads over heads.  Returns (seconds, threads)."""
-    import torch
-    import oracle
-    from kda_gated_delta_gb300 import workloads
-
-    if "inp" not in _PREFILL_HOST:
-        _PREFILL_HOST["inp"] = workloads.workload_inputs(1)
-    inp = _PREFILL_HOST["inp"]
-    n = int(n_tokens)
-    sub = {k: inp[k][:n] for k in ("q", "k", "v", "g_raw", "b_raw")}
-    cu = torch.tensor([0, n], dtype=torch.int32)
-    sidx = inp["state_idx"][:1]
-    pool = inp["pool"][sidx.long()]
-    threads = min(len(os.sched_getaffinity(0)), 32)
-    p = oracle.make_params(32, 128)
-    t0 = time.perf_counter()
-    oracle.forward(p, sub["q"], sub["k"], sub["v"], sub["g_raw"], sub["b_raw"], inp["A_log"], inp["dt_bias"],
-                   cu, pool, torch.zeros(1, dtype=torch.int32), nthreads=threads)
-    return time.perf_counter() - t0, threads
-
-
 def oracle_workload_once():
     """Oracle over the whole varlen workload (8 sequences, all 32 heads, threads over heads)."""
     import oracle
@@ -261,28 +245,32 @@ def cpu_baseline(target_s=10.0):
 
 
 def run_reference(args):
+    """The reference arm of this build: the fp64 oracle (the pages carry no runnable reference),
+    timed as it stands on the host cores over the same varlen workload as our arm's headline,
+    one whole workload per step."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     import oracle
     oracle.build()
-    n = 128
     for _ in range(args.warmup):
-        oracle_prefill_sample(n)
-    times, thr = [], 1
+        oracle_workload_once()
+    times, thr, T = [], 1, 0
     for _ in range(args.steps):
-        t, thr = oracle_prefill_sample(n)
+        t, thr, T = oracle_workload_once()
         times.append(t)
     total = sum(times)
-    value = n * args.steps / total
+    value = T * args.steps / total
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": "varlen_prefill_bf16 (sampled: first 128 tokens of sequence 0, 32 heads)",
-                       "num_heads": 32, "head_dim": 128, "chunk_size": 64},
+            "config": {"workload": f"varlen_prefill_bf16: 8 seqs, lengths U[512,4096] (seed 1001), T={T}, "
+                                   "H=32, d=128, chunk 64",
+                       "io_dtype": "bf16", "tokens_per_step": T},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
-                             "sample": f"{n} tokens x 32 heads per step, fp64 token recurrence"},
+                             "sample": f"fp64 token recurrence over the whole varlen workload ({T} tokens, "
+                                       f"8 sequences, 32 heads, threads over heads) per step"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -291,6 +279,89 @@ def run_reference(args):
 # ---------------------------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------------------------
+def _tiny_latency(kda, workloads, dev, reps=200):
+    """The tiny fp32 prefill (1 sequence of 64 tokens, H = 2, d = 16, chunk 16): a launch-latency
+    figure, in microseconds per call, on the device (events around back-to-back calls) and on the
+    host (wall clock per call including the synchronisation at the end)."""
+    import torch
+    w = workloads.workload(0)
+    inp = workloads.to_device(workloads.workload_inputs(0), dev)
+    p = kda.make_params(w.num_heads, w.head_dim, io_dtype=torch.float32, out_dtype=torch.float32,
+                        chunk_size=w.chunk_size)
+    T = int(inp["cu_seqlens"][-1])
+    ws = torch.empty(kda.prefill_workspace_size(p, 1, T), dtype=torch.uint8, device=dev)
+    out = torch.empty(T, w.num_heads, w.head_dim, dtype=torch.float32, device=dev)
+    pool = inp["pool"].clone()
+
+    def call():
+        kda.chunk_prefill(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["b_raw"], inp["A_log"], inp["dt_bias"],
+                          inp["cu_seqlens"], pool, inp["state_idx"], out, params=p, workspace=ws)
+
+    for _ in range(20):
+        call()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    a.record()
+    for _ in range(reps):
+        call()
+    b.record()
+    torch.cuda.synchronize()
+    host_us = 1e6 * (time.perf_counter() - t0) / reps
+    dev_us = 1e3 * a.elapsed_time(b) / reps
+    return {"us_per_call": round(dev_us, 2), "host_us_per_call": round(host_us, 2), "launches_per_call": 3,
+            "calls": reps, "workload": "tiny_prefill_fp32: 1 seq T=64, H=2, d=16, chunk 16, fp32 in/out",
+            "bound": "launch latency (no roofline)"}
+
+
+def _long_prefill(kda, workloads, dev, roof, reps=2):
+    """The long prefill: 1 sequence of 131072 tokens as 32 successive 4096-token calls carrying
+    the state in one slot (bf16 in and out, chunk 64).  One untimed pass, then ``reps`` timed
+    passes; every call is timed with events on the launching stream."""
+    import torch
+    w = workloads.workload(3)
+    H, D, per = w.num_heads, w.head_dim, 4096
+    host = workloads.workload_inputs(3)
+    d = workloads.to_device(host, dev)
+    del host
+    p = kda.make_params(H, D, io_dtype=torch.bfloat16, out_dtype=torch.bfloat16, chunk_size=64)
+    ws = torch.empty(kda.prefill_workspace_size(p, 1, per), dtype=torch.uint8, device=dev)
+    out = torch.empty(per * w.calls, H, D, dtype=torch.bfloat16, device=dev)
+    cu = torch.tensor([0, per], dtype=torch.int32, device=dev)
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(w.calls)] for _ in range(reps + 1)]
+    for e in [x for r in evs for c in r for x in c]:
+        e.record()
+    torch.cuda.synchronize()
+    for r in range(reps + 1):
+        pool = d["pool"].clone()
+        for c in range(w.calls):
+            s = slice(c * per, (c + 1) * per)
+            kda.chunk_prefill(d["q"][s], d["k"][s], d["v"][s], d["g_raw"][s], d["b_raw"][s], d["A_log"],
+                              d["dt_bias"], cu, pool, d["state_idx"], out[s], params=p, workspace=ws, events=evs[r][c])
+    torch.cuda.synchronize()
+    call_ms, phase = [], [0.0, 0.0, 0.0]
+    for r in range(1, reps + 1):
+        for c in range(w.calls):
+            e = evs[r][c]
+            call_ms.append(e[0].elapsed_time(e[3]))
+            for j in range(3):
+                phase[j] += e[j].elapsed_time(e[j + 1])
+    n = len(call_ms)
+    ms_call = sum(call_ms) / n
+    per_call_B = prefill_bytes(per, 1, H, D, 2, 2)
+    rf = roof(per_call_B, ms_call, ("kda_chunk_table", "kda_chunk_intra", "kda_chunk_state"))
+    rf["traffic"] = None                       # the stored capture is of the varlen workload
+    rf["scope"] = "one 4096-token call: its token inputs and output, the carried state read and written once"
+    return {"value": round(per * w.calls / (ms_call * 1e-3 * w.calls), 1), "unit": UNIT,
+            "ms_per_call": round(ms_call, 5), "ms_per_call_median": round(statistics.median(call_ms), 5),
+            "ms_total": round(ms_call * w.calls, 4), "calls": w.calls, "tokens_per_call": per,
+            "phase_ms_per_call": {"kda_chunk_table": round(phase[0] / n, 5), "kda_chunk_intra": round(phase[1] / n, 5),
+                                  "kda_chunk_state": round(phase[2] / n, 5)},
+            "roofline": rf,
+            "workload": "long_chunked_prefill_bf16: 1 seq T=131072 as 32 calls x 4096 carrying the state, "
+                        "H=32, d=128, chunk 64, bf16 in/out"}
+
+
 def run_ours(args):
     import torch
 
@@ -306,46 +377,54 @@ def run_ours(args):
 
     bw_peak, _, peak_src = peaks()
     H, D = 32, 128
+    only_prefill = args.only == "prefill"
 
     # ---- inputs, resident in HBM --------------------------------------------------------------
     wp, wd, wv = workloads.workload(1), workloads.workload(2), workloads.workload(4)
     pre_h = workloads.workload_inputs(1)
-    dec_h = workloads.workload_inputs(2)
-    ver_h = workloads.workload_inputs(4)
-    pre, dec, ver = (workloads.to_device(x, dev) for x in (pre_h, dec_h, ver_h))
+    pre = workloads.to_device(pre_h, dev)
     T = int(pre_h["cu_seqlens"][-1])
     Np = len(wp.lengths)
     p_pre = kda.make_params(H, D, io_dtype=torch.bfloat16, out_dtype=torch.bfloat16, chunk_size=64)
-    p_dec = kda.make_params(H, D, io_dtype=torch.bfloat16, out_dtype=torch.bfloat16)
-    p_ver = kda.make_params(H, D, io_dtype=torch.bfloat16, out_dtype=torch.bfloat16, gate="gdn")
     ws = torch.empty(kda.prefill_workspace_size(p_pre, Np, T), dtype=torch.uint8, device=dev)
     out_pre = torch.empty(T, H, D, dtype=torch.bfloat16, device=dev)
-    out_dec = torch.empty(wd.batch, H, D, dtype=torch.bfloat16, device=dev)
-    out_ver = torch.empty(wv.batch * wv.t_draft, H, D, dtype=torch.bfloat16, device=dev)
-    inter = torch.empty(wv.batch, wv.t_draft, H, D, D, dtype=torch.float32, device=dev)
-    # buffered (ReplaySSM) decode on the decode workload: ring length 8 (the length the pages'
-    # microbenchmark used), cursors staggered across requests so 1/8 of the rows flush per step
-    RL = 8
-    rpool = dec["pool"].clone()
-    rings = kda.replay_rings(rpool.shape[0], H, D, RL, device=dev)
-    rpos = [torch.tensor([(t + b) % RL for b in range(wd.batch)], dtype=torch.int32, device=dev) for t in range(RL)]
-    out_rep = torch.empty(wd.batch, H, D, dtype=torch.bfloat16, device=dev)
+    RLS = (8, 16)
+    if not only_prefill:
+        dec = workloads.to_device(workloads.workload_inputs(2), dev)
+        ver = workloads.to_device(workloads.workload_inputs(4), dev)
+        p_dec = kda.make_params(H, D, io_dtype=torch.bfloat16, out_dtype=torch.bfloat16)
+        p_ver = kda.make_params(H, D, io_dtype=torch.bfloat16, out_dtype=torch.bfloat16, gate="gdn")
+        out_dec = torch.empty(wd.batch, H, D, dtype=torch.bfloat16, device=dev)
+        out_ver = torch.empty(wv.batch * wv.t_draft, H, D, dtype=torch.bfloat16, device=dev)
+        inter = torch.empty(wv.batch, wv.t_draft, H, D, D, dtype=torch.float32, device=dev)
+        # buffered (ReplaySSM) decode on the decode workload at ring lengths 8 (the pages'
+        # microbenchmark) and 16 (the pages' default); cursors staggered across requests so that
+        # 1/L of the rows flush per step
+        rep = {}
+        for RL in RLS:
+            rpool = dec["pool"].clone()
+            rep[RL] = dict(pool=rpool, rings=kda.replay_rings(rpool.shape[0], H, D, RL, device=dev),
+                           pos=[torch.tensor([(t + b) % RL for b in range(wd.batch)], dtype=torch.int32, device=dev)
+                                for t in range(RL)],
+                           out=torch.empty(wd.batch, H, D, dtype=torch.bfloat16, device=dev))
 
     K, W = args.steps, args.warmup
     ev = lambda: torch.cuda.Event(enable_timing=True)
     pre_ev = [[ev() for _ in range(4)] for _ in range(K + W)]
     dec_ev = [[ev(), ev()] for _ in range(K + W)]
     ver_ev = [[ev(), ev()] for _ in range(K + W)]
-    rep_ev = [[ev(), ev()] for _ in range(K + W)]
+    rep_ev = {RL: [[ev(), ev()] for _ in range(K + W)] for RL in RLS}
     for e in [x for row in pre_ev for x in row]:
         e.record()          # create the underlying CUDA events before handing them to the library
     torch.cuda.synchronize()
-    launches_per_step = 3 + 1 + 1 + 1
+    launches_per_step = 3 if only_prefill else 3 + 1 + 1 + len(RLS)
 
     def step(i):
         kda.chunk_prefill(pre["q"], pre["k"], pre["v"], pre["g_raw"], pre["b_raw"], pre["A_log"],
                           pre["dt_bias"], pre["cu_seqlens"], pre["pool"], pre["state_idx"], out_pre,
                           params=p_pre, workspace=ws, events=pre_ev[i])
+        if only_prefill:
+            return
         dec_ev[i][0].record()
         kda.recurrent_decode(dec["q"], dec["k"], dec["v"], dec["g_raw"], dec["b_raw"], dec["A_log"],
                              dec["dt_bias"], dec["pool"], dec["state_idx"], out_dec, params=p_dec)
@@ -355,10 +434,13 @@ def run_ours(args):
                              ver["dt_bias"], ver["pool"], ver["state_idx"], wv.t_draft, inter, out_ver,
                              params=p_ver)
         ver_ev[i][1].record()
-        rep_ev[i][0].record()
-        kda.replay_decode(dec["q"], dec["k"], dec["v"], dec["g_raw"], dec["b_raw"], dec["A_log"], dec["dt_bias"],
-                          rpool, dec["state_idx"], rings, rpos[i % RL], None, out_rep, params=p_dec)
-        rep_ev[i][1].record()
+        for RL in RLS:
+            r = rep[RL]
+            rep_ev[RL][i][0].record()
+            kda.replay_decode(dec["q"], dec["k"], dec["v"], dec["g_raw"], dec["b_raw"], dec["A_log"],
+                              dec["dt_bias"], r["pool"], dec["state_idx"], r["rings"], r["pos"][i % RL], None,
+                              r["out"], params=p_dec)
+            rep_ev[RL][i][1].record()
 
     for i in range(W):
         step(K + i)
@@ -384,24 +466,6 @@ def run_ours(args):
     barrier(dist)
     clk = clocks.stop()
 
-    step_ms = reduce_max(dist, t_start.elapsed_time(t_end) / K, dev)
-    ph = [[pre_ev[i][j].elapsed_time(pre_ev[i][j + 1]) for j in range(3)] for i in range(K)]
-    phase_ms = [sum(r[j] for r in ph) / K for j in range(3)]
-    pre_ms = reduce_max(dist, sum(phase_ms), dev)
-    phase_max = [reduce_max(dist, m, dev) for m in phase_ms]
-    dec_ms = reduce_max(dist, sum(dec_ev[i][0].elapsed_time(dec_ev[i][1]) for i in range(K)) / K, dev)
-    ver_ms = reduce_max(dist, sum(ver_ev[i][0].elapsed_time(ver_ev[i][1]) for i in range(K)) / K, dev)
-    rep_ms = reduce_max(dist, sum(rep_ev[i][0].elapsed_time(rep_ev[i][1]) for i in range(K)) / K, dev)
-
-    pre_B = prefill_bytes(T, Np, H, D, 2, 2)
-    dec_B = decode_bytes(wd.batch, H, D, 2, 2)
-    ver_B = verify_bytes(wv.batch, wv.t_draft, H, D, 2, 2)
-    value = world * T / (pre_ms * 1e-3)
-    dec_value = world * wd.batch / (dec_ms * 1e-3)
-    ver_value = world * wv.batch * wv.t_draft / (ver_ms * 1e-3)
-    rep_B = sum(replay_bytes(rpos[i % RL].tolist(), RL, H, D, 2, 2) for i in range(K)) / K
-    rep_value = world * wd.batch / (rep_ms * 1e-3)
-
     def roof(bytes_, ms, kernels_):
         ach = bytes_ / (ms * 1e-3) / 1e9
         tr = [measured_traffic(k) for k in kernels_]
@@ -410,11 +474,55 @@ def run_ours(args):
                 "algorithmic_bytes": bytes_,
                 "traffic": None if any(t is None for t in tr) else sum(tr)}
 
+    step_ms = reduce_max(dist, t_start.elapsed_time(t_end) / K, dev)
+    ph = [[pre_ev[i][j].elapsed_time(pre_ev[i][j + 1]) for j in range(3)] for i in range(K)]
+    phase_ms = [sum(r[j] for r in ph) / K for j in range(3)]
+    pre_ms = reduce_max(dist, sum(phase_ms), dev)
+    phase_max = [reduce_max(dist, m, dev) for m in phase_ms]
+    pre_B = prefill_bytes(T, Np, H, D, 2, 2)
+    value = world * T / (pre_ms * 1e-3)
+
     kernels = [{"name": n, "ms": round(m, 5)} for n, m in
                zip(("kda_chunk_table", "kda_chunk_intra", "kda_chunk_state"), phase_ms)]
-    kernels += [{"name": "kda_recurrent_decode", "ms": round(dec_ms, 5)},
-                {"name": "kda_recurrent_verify", "ms": round(ver_ms, 5)},
-                {"name": "kda_replay_decode", "ms": round(rep_ms, 5)}]
+    per_kernel = {
+        "kda_chunk_intra": (intra_bytes(T, H, D, 2), phase_max[1],
+                            "token inputs read once (q, k, v bf16; g_raw, b_raw fp32); its record is workspace"),
+        "kda_chunk_state": (state_pass_bytes(T, Np, H, D, 2), phase_max[2],
+                            "states read and written once, output written once; the record it reads is workspace"),
+    }
+    extra = {}
+    if not only_prefill:
+        dec_ms = reduce_max(dist, sum(dec_ev[i][0].elapsed_time(dec_ev[i][1]) for i in range(K)) / K, dev)
+        ver_ms = reduce_max(dist, sum(ver_ev[i][0].elapsed_time(ver_ev[i][1]) for i in range(K)) / K, dev)
+        rep_ms = {RL: reduce_max(dist, sum(rep_ev[RL][i][0].elapsed_time(rep_ev[RL][i][1]) for i in range(K)) / K, dev)
+                  for RL in RLS}
+        dec_B = decode_bytes(wd.batch, H, D, 2, 2)
+        ver_B = verify_bytes(wv.batch, wv.t_draft, H, D, 2, 2)
+        rep_B = {RL: sum(replay_bytes(rep[RL]["pos"][i % RL].tolist(), RL, H, D, 2, 2) for i in range(K)) / K
+                 for RL in RLS}
+        kernels += [{"name": "kda_recurrent_decode", "ms": round(dec_ms, 5)},
+                    {"name": "kda_recurrent_verify", "ms": round(ver_ms, 5)}]
+        kernels += [{"name": f"kda_replay_decode_l{RL}", "ms": round(rep_ms[RL], 5)} for RL in RLS]
+        per_kernel["kda_recurrent_decode"] = (dec_B, dec_ms, "decode workload bytes")
+        per_kernel["kda_recurrent_verify"] = (ver_B, ver_ms, "verify workload bytes")
+        for RL in RLS:
+            per_kernel[f"kda_replay_decode_l{RL}"] = (rep_B[RL], rep_ms[RL],
+                                                      "buffered decode bytes (averaged over the timed steps)")
+        extra["decode"] = {"value": round(world * wd.batch / (dec_ms * 1e-3), 1), "unit": UNIT, "ms": round(dec_ms, 5),
+                           "state_gbs": round(wd.batch * H * 2 * D * D * 4 / (dec_ms * 1e-3) / 1e9, 1),
+                           "roofline": roof(dec_B, dec_ms, ("kda_recurrent_decode",)),
+                           "workload": "decode_bf16: 256 requests x 1 token, H=32, d=128, 512-slot fp32 pool"}
+        extra["verify"] = {"value": round(world * wv.batch * wv.t_draft / (ver_ms * 1e-3), 1), "unit": UNIT,
+                           "ms": round(ver_ms, 5), "roofline": roof(ver_B, ver_ms, ("kda_recurrent_verify",)),
+                           "workload": "gdn_verify_bf16: 64 requests x 4 drafts, per-head gate, inter states"}
+        for RL in RLS:
+            key = "decode_replay" if RL == 8 else f"decode_replay_l{RL}"
+            extra[key] = {"value": round(world * wd.batch / (rep_ms[RL] * 1e-3), 1), "unit": UNIT,
+                          "ms": round(rep_ms[RL], 5), "ring_len": RL,
+                          "speedup_vs_decode": round(dec_ms / rep_ms[RL], 3),
+                          "roofline": roof(rep_B[RL], rep_ms[RL], (f"kda_replay_decode_l{RL}",)),
+                          "workload": f"decode_bf16 through the buffered decode: ring {RL}, cursors staggered, "
+                                      f"1/{RL} of the rows flush per step (averaged over the timed steps)"}
     tot = sum(k["ms"] for k in kernels)
     for k in kernels:
         k["share"] = round(k["ms"] / tot, 4)
@@ -424,15 +532,6 @@ def run_ours(args):
     call_roof.update({"scope": "prefill call (chunk_table + chunk_intra + chunk_state), varlen workload",
                       "ms": round(pre_ms, 5)})
     # the dominant kernel's own roofline: its algorithmic bytes over its own event-timed duration
-    per_kernel = {
-        "kda_chunk_intra": (intra_bytes(T, H, D, 2), phase_max[1],
-                            "token inputs read once (q, k, v bf16; g_raw, b_raw fp32); its record is workspace"),
-        "kda_chunk_state": (state_pass_bytes(T, Np, H, D, 2), phase_max[2],
-                            "states read and written once, output written once; the record it reads is workspace"),
-        "kda_recurrent_decode": (dec_B, dec_ms, "decode workload bytes"),
-        "kda_recurrent_verify": (ver_B, ver_ms, "verify workload bytes"),
-        "kda_replay_decode": (rep_B, rep_ms, "buffered decode bytes (averaged over the timed steps)"),
-    }
     if dominant["name"] in per_kernel:
         b_, ms_, what = per_kernel[dominant["name"]]
         roofline = roof(b_, ms_, (dominant["name"],))
@@ -446,7 +545,7 @@ def run_ours(args):
     # buffers).  Consecutive steps are pipelined on three streams with two device buffer sets: the
     # inputs of step i + 1 travel while step i computes and the output of step i - 1 travels back.
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not only_prefill:
         names = ("q", "k", "v", "g_raw", "b_raw", "cu_seqlens", "state_idx")
         host = {k: pre_h[k].pin_memory() for k in names}
         host_out = torch.empty(T, H, D, dtype=torch.bfloat16).pin_memory()
@@ -507,8 +606,16 @@ def run_ours(args):
 
     if rank != 0:
         return 0
+    if not only_prefill:
+        # single-GPU figures outside the timed steps: launch latency and the long chunked prefill
+        del dec, ver, inter, rep
+        torch.cuda.empty_cache()
+        extra["tiny"] = _tiny_latency(kda, workloads, dev)
+        extra["long_prefill"] = _long_prefill(kda, workloads, dev, roof)
+        if kda.check_device_errors() != 0:
+            raise RuntimeError("device error recorded in the tiny or long prefill")
     cpu = None
-    if not args.no_cpu_baseline and world == 1:
+    if not args.no_cpu_baseline and world == 1 and not only_prefill:
         cpu = cpu_baseline()
 
     line = {
@@ -520,17 +627,7 @@ def run_ours(args):
                    "io_dtype": "bf16", "out_dtype": "bf16", "state_dtype": "f32", "tokens_per_step": T,
                    "l2": "no flush: every working set > 129 MB L2", "parallelism": f"replicas x{world}"},
         "roofline": roofline,
-        "decode": {"value": round(dec_value, 1), "unit": UNIT, "ms": round(dec_ms, 5),
-                   "state_gbs": round(wd.batch * H * 2 * D * D * 4 / (dec_ms * 1e-3) / 1e9, 1),
-                   "roofline": roof(dec_B, dec_ms, ("kda_recurrent_decode",)),
-                   "workload": "decode_bf16: 256 requests x 1 token, H=32, d=128, 512-slot fp32 pool"},
-        "verify": {"value": round(ver_value, 1), "unit": UNIT, "ms": round(ver_ms, 5),
-                   "roofline": roof(ver_B, ver_ms, ("kda_recurrent_verify",)),
-                   "workload": "gdn_verify_bf16: 64 requests x 4 drafts, per-head gate, inter states"},
-        "decode_replay": {"value": round(rep_value, 1), "unit": UNIT, "ms": round(rep_ms, 5), "ring_len": RL,
-                          "roofline": roof(rep_B, rep_ms, ("kda_replay_decode",)),
-                          "workload": "decode_bf16 through the buffered decode: ring 8, cursors staggered, "
-                                      "1/8 of the rows flush per step (averaged over the timed steps)"},
+        **extra,
         "kernels": kernels,
         "clocks": clk,
         "e2e": e2e,
@@ -549,6 +646,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="all", choices=["all", "prefill"],
+                    help="prefill: the varlen prefill alone, for profiler captures")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

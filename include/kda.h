@@ -252,16 +252,19 @@ int32_t kda_commit_verified_states(const kda_params* p,
  * kda_chunk_prefill asks for.
  *
  * What it does: exactly the work of kda_chunk_prefill, with the same arguments minus the
- * workspace.  Its scratch is a fixed array of KDA_STATIC_SCRATCH_BYTES compiled into the library;
- * every GPU that loads the library holds that much device memory for it until the process exits.
- * The call allocates nothing.  A problem whose kda_chunk_prefill_workspace_size(...) exceeds
+ * workspace, and the same host-side checks.  Its scratch is a fixed array of
+ * KDA_STATIC_SCRATCH_BYTES compiled into the library.  A device holds that much memory for it
+ * until its context is destroyed (normally at process exit): under CUDA's default lazy module
+ * loading from the first call of this entry point on that device, under eager loading
+ * (CUDA_MODULE_LOADING=EAGER) from the creation of the context.  The call allocates nothing.  A problem whose kda_chunk_prefill_workspace_size(...) exceeds
  * KDA_STATIC_SCRATCH_BYTES is rejected with KDA_ERR_SCRATCH_LIMIT before any work is enqueued
  * (with H = 32, head_dim = 128, chunk 64 the array covers ceil(T / 64) + num_seqs <= 56 chunks,
  * about 3,000 tokens per call).
  *
- * The first call on each device looks up the device address of the array (this can load the
- * library's device code on that device); make that first call outside any stream capture.
- * All calls share the one array and it keeps whatever the last call left in it (nothing in it
+ * Every call looks up the device address of the array in the current context (nothing is
+ * cached, so a context that was reset and created again is handled); under lazy loading the
+ * first call on a device also loads the library's device code there, so make that first call
+ * outside any stream capture.  All calls share the one array and it keeps whatever the last call left in it (nothing in it
  * needs to start at zero).  Calls whose kernels overlap on the GPU, on different streams or
  * from different host threads, race on the array and produce garbage: order them.
  */

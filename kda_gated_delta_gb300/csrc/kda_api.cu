@@ -12,17 +12,6 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-kda::GateParams gate_params(const kda_params& p)
-{
-    kda::GateParams g;
-    g.scale = p.scale > 0.f ? p.scale : 1.0f / sqrtf((float)p.head_dim);
-    g.l2_eps = p.l2_eps;
-    g.softplus_threshold = p.softplus_threshold;
-    g.lower_bound = p.lower_bound;
-    g.use_lower_bound = p.use_lower_bound ? 1 : 0;
-    return g;
-}
-
 // Checks shared by all entry points; `tokens` is the number of input rows.
 int32_t check_common(const kda_params* p, const void* q, const void* k, const void* v,
                      const float* g_raw, const float* b_raw, const float* A_log,
@@ -43,7 +32,44 @@ int32_t check_common(const kda_params* p, const void* q, const void* k, const vo
 
 int32_t from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
+using kda::gate_params;
+
 }  // namespace
+
+namespace kda {
+
+GateParams gate_params(const kda_params& p)
+{
+    GateParams g;
+    g.scale = p.scale > 0.f ? p.scale : 1.0f / sqrtf((float)p.head_dim);
+    g.l2_eps = p.l2_eps;
+    g.softplus_threshold = p.softplus_threshold;
+    g.lower_bound = p.lower_bound;
+    g.use_lower_bound = p.use_lower_bound ? 1 : 0;
+    return g;
+}
+
+int32_t check_prefill(const kda_params* p, const void* q, const void* k, const void* v, const float* g_raw,
+                      const float* b_raw, const float* A_log, const float* dt_bias, const int32_t* cu_seqlens,
+                      int32_t num_seqs, int64_t total_tokens, const void* state_pool, int64_t num_slots,
+                      const int32_t* state_idx, const void* out, bool* noop)
+{
+    *noop = false;
+    if (num_seqs < 0) return KDA_ERR_INVALID_ARG;
+    const int32_t rc = check_common(p, q, k, v, g_raw, b_raw, A_log, dt_bias, total_tokens, state_pool,
+                                    num_slots, state_idx, out);
+    if (rc != KDA_OK) return rc;
+    if (!prefill_supported(*p)) return KDA_ERR_UNSUPPORTED;
+    if (total_tokens == 0 || num_seqs == 0) {
+        *noop = true;
+        return KDA_OK;
+    }
+    if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
+    if (total_tokens >= ((int64_t)1 << 31) - 64) return KDA_ERR_UNSUPPORTED;
+    return KDA_OK;
+}
+
+}  // namespace kda
 
 extern "C" {
 
@@ -93,14 +119,10 @@ int32_t prefill_impl(const kda_params* p, const void* q, const void* k, const vo
                      size_t workspace_bytes, kda_stream_t stream, const cudaEvent_t* events,
                      float* chunk_states = nullptr, int64_t chunk_states_capacity = 0)
 {
-    if (num_seqs < 0) return KDA_ERR_INVALID_ARG;
-    int32_t rc = check_common(p, q, k, v, g_raw, b_raw, A_log, dt_bias, total_tokens, state_pool,
-                              num_slots, state_idx, out);
-    if (rc != KDA_OK) return rc;
-    if (!kda::prefill_supported(*p)) return KDA_ERR_UNSUPPORTED;
-    if (total_tokens == 0 || num_seqs == 0) return KDA_OK;
-    if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
-    if (total_tokens >= ((int64_t)1 << 31) - 64) return KDA_ERR_UNSUPPORTED;
+    bool noop = false;
+    const int32_t rc = kda::check_prefill(p, q, k, v, g_raw, b_raw, A_log, dt_bias, cu_seqlens, num_seqs,
+                                          total_tokens, state_pool, num_slots, state_idx, out, &noop);
+    if (rc != KDA_OK || noop) return rc;
     const size_t need = kda::prefill_workspace_bytes(*p, num_seqs, total_tokens);
     if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return KDA_ERR_WORKSPACE;

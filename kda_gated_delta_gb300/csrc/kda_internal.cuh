@@ -58,6 +58,18 @@ __device__ __forceinline__ float gate_log_decay(float x, float rate, const GateP
 
 __device__ __forceinline__ float sigmoid_f32(float x) { return 1.0f / (1.0f + expf(-x)); }
 
+// ---- host-side argument handling (kda_api.cu) ----------------------------------------------------
+GateParams gate_params(const kda_params& p);
+// The host-side checks of a chunk-prefill call, in one place for every prefill entry point (the
+// caller-workspace variants and the static-scratch one), so that they cannot drift apart.
+// Returns KDA_OK or the negative status of the first failed check; *noop is set when the call is
+// valid but has nothing to do (T = 0 or num_seqs = 0).  The workspace or scratch size is checked
+// by the caller, after this.
+int32_t check_prefill(const kda_params* p, const void* q, const void* k, const void* v, const float* g_raw,
+                      const float* b_raw, const float* A_log, const float* dt_bias, const int32_t* cu_seqlens,
+                      int32_t num_seqs, int64_t total_tokens, const void* state_pool, int64_t num_slots,
+                      const int32_t* state_idx, const void* out, bool* noop);
+
 // ---- launchers (implemented in kda_recurrent.cu / kda_prefill.cu) ------------------------------
 cudaError_t launch_recurrent(const kda_params& p, const GateParams& gp, const void* q,
                              const void* k, const void* v, const float* g_raw,

@@ -69,9 +69,11 @@ def workload(wid: int) -> Workload:
 
 def make_inputs(lengths, num_heads, head_dim, io_dtype, *, gate="kda", pool_slots=1,
                 pool_std=0.0, seed=0, dt_bias_std=0.0, padding_rows=(), state_idx=None,
-                q_std=1.0, g_mean=0.0, g_std=1.0, b_mean=0.0, b_std=1.0):
+                q_std=1.0, g_mean=0.0, g_std=1.0, b_mean=0.0, b_std=1.0,
+                A_log_range=(0.0, math.log(16.0))):
     """Random host inputs for packed sequences of the given lengths.
 
+    ``A_log_range`` = (lo, hi) draws A_log ~ U(lo, hi) (default U(0, ln 16)).
     Returns a dict of CPU tensors: q, k, v [T,H,D] (io_dtype); g_raw [T,H,D] or [T,H]; b_raw [T,H];
     A_log [H]; dt_bias [H,D] or [H]; cu_seqlens [N+1] int32; pool [slots,H,D,D] fp32;
     state_idx [N] int32 (entries listed in ``padding_rows`` set to -1).
@@ -90,7 +92,10 @@ def make_inputs(lengths, num_heads, head_dim, io_dtype, *, gate="kda", pool_slot
     gshape = (T, H, D) if gate == "kda" else (T, H)
     g_raw = randn(*gshape) * g_std + g_mean
     b_raw = randn(T, H) * b_std + b_mean
-    A_log = torch.rand(H, generator=gen, dtype=torch.float32) * math.log(16.0)
+    lo, hi = float(A_log_range[0]), float(A_log_range[1])
+    A_log = torch.rand(H, generator=gen, dtype=torch.float32) * (hi - lo)
+    if lo != 0.0:
+        A_log = A_log + lo
     dshape = (H, D) if gate == "kda" else (H,)
     dt_bias = randn(*dshape) * dt_bias_std if dt_bias_std > 0 else torch.zeros(dshape, dtype=torch.float32)
     if pool_std > 0:

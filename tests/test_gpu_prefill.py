@@ -1,15 +1,21 @@
 """GPU parity of kda_chunk_prefill against the fp64 oracle through the C ABI: the tiny fp32
 workload, edge shapes (single tokens, chunk-boundary lengths, ragged varlen, padding rows,
-empty sequences), the full varlen workload, the long prefill split into 32 calls carrying the
-state (sampled heads), and the mode invariances (prefill then decode equals one prefill;
-chunked calls equal one call; packed varlen equals separate calls)."""
+empty sequences), gate extremes on both kernel pairs (decays from ~1e-3 per token to underflow,
+and g_raw + dt_bias above the softplus threshold of 20), the full varlen workload, the long
+prefill split into 32 calls carrying the state (all heads, every call), and the mode invariances
+(prefill then decode equals one prefill; chunked calls equal one call; packed varlen equals
+separate calls).  The full workloads are also checked per (sequence, head), each block normalised
+by its own largest reference value."""
+import math
+
 import numpy as np
 import pytest
 import torch
 
 import kda_gated_delta_gb300 as kda
 from kda_gated_delta_gb300 import workloads
-from helpers import np64, oracle_run, rel_err, tol_for
+import oracle
+from helpers import NTHREADS, PER_HEAD_BF16, np64, oracle_run, per_head_err, rel_err, tol_for
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -104,6 +110,35 @@ def test_mild_and_strong_gates_fp32():
         check(inp, H, D, 64, torch.float32)
 
 
+@pytest.mark.parametrize("g_mean", [-8.0, 4.0])
+def test_mild_and_strong_gates_tensor_core(g_mean):
+    """The same gate extremes on the tensor-core pair (bf16, d = 128, chunk 64): fp16 Gram
+    operands, the special-function gate and the tf32 record meet g ~ -1e-3 per token (g_raw ~
+    N(-8, 2)) and decays that underflow within a few tokens (g_raw ~ N(4, 2), rates up to 16)."""
+    H, D = 4, 128
+    inp = workloads.make_inputs([300, 130, 64, 7], H, D, torch.bfloat16, pool_slots=5, pool_std=0.05,
+                                seed=70 + int(g_mean), g_mean=g_mean, g_std=2.0)
+    check(inp, H, D, 64, torch.bfloat16)
+
+
+def threshold_inputs(lengths, H, D, io, seed, gate="kda", pool_slots=4):
+    """g_raw + dt_bias ~ N(21, 3^2 + 1): most values above the softplus threshold of 20, some
+    below it.  Small rates (A_log ~ U(ln 0.005, ln 0.05)) keep the decays moderate (g ~ -0.1 ..
+    -1.5 per token), so the branch taken above the threshold decides real outputs."""
+    return workloads.make_inputs(lengths, H, D, io, gate=gate, pool_slots=pool_slots, pool_std=0.05, seed=seed,
+                                 g_mean=21.0, g_std=3.0, dt_bias_std=1.0,
+                                 A_log_range=(math.log(0.005), math.log(0.05)))
+
+
+@pytest.mark.parametrize("io,C,D", [(torch.float32, 32, 64), (torch.bfloat16, 64, 128)])
+def test_softplus_threshold_both_pairs(io, C, D):
+    H = 3
+    inp = threshold_inputs([150, 70, 1], H, D, io, seed=C + D)
+    x = inp["g_raw"] + inp["dt_bias"][None]
+    assert (x > 20).float().mean() > 0.5 and (x <= 20).any()
+    check(inp, H, D, C, io)
+
+
 def test_safe_gate_and_bf16_output():
     H, D = 4, 128
     inp = workloads.make_inputs([300, 45], H, D, torch.bfloat16, pool_slots=4, pool_std=0.05, seed=12,
@@ -118,31 +153,59 @@ def test_varlen_workload_full():
     o_ref, p_ref, _ = oracle_run(inp, 32, 128)
     assert rel_err(np64(out), o_ref) <= tol_for(torch.bfloat16, torch.float32)
     assert rel_err(np64(pool), p_ref) <= tol_for(torch.bfloat16, torch.float32)
+    # per (sequence, head), each normalised by its own largest reference value
+    used = inp["state_idx"].long()
+    e_oh = per_head_err(np64(out), o_ref, inp["cu_seqlens"].tolist())
+    e_sh = per_head_err(np64(pool)[used], p_ref[used])
+    print(f"varlen prefill per-head worst: output {e_oh:.3e}, state {e_sh:.3e}")
+    assert e_oh <= PER_HEAD_BF16 and e_sh <= PER_HEAD_BF16, (e_oh, e_sh)
     out_b, _ = run_prefill(inp, 64, out_dtype=torch.bfloat16)
     assert rel_err(np64(out_b), o_ref) <= tol_for(torch.bfloat16, torch.bfloat16)
 
 
-def test_long_chunked_prefill_sampled_heads():
+def test_long_chunked_prefill_all_heads():
     """1 sequence of 131072 tokens as 32 successive 4096-token calls carrying the state in one
-    slot; heads 0 and 19 are compared against the oracle over the whole sequence."""
+    slot.  The oracle runs the same 32 calls carrying its own fp64 state; every head is compared,
+    for the output of every call and the state after every call (tensor-wide and per head)."""
     w = workloads.workload(3)
     inp = workloads.workload_inputs(3)
     d = workloads.to_device(inp, DEV)
+    H, D = w.num_heads, w.head_dim
     pool = d["pool"].clone()
     T, per = 131072, 4096
-    out = torch.empty(T, 32, 128, device=DEV, dtype=torch.float32)
+    assert w.calls * per == T
+    out = torch.empty(T, H, D, device=DEV, dtype=torch.float32)
     cu = torch.tensor([0, per], dtype=torch.int32, device=DEV)
-    ws = torch.empty(kda.prefill_workspace_size(kda.make_params(32, 128), 1, per), dtype=torch.uint8, device=DEV)
+    ws = torch.empty(kda.prefill_workspace_size(kda.make_params(H, D), 1, per), dtype=torch.uint8, device=DEV)
+    states = []
     for c in range(w.calls):
         s = slice(c * per, (c + 1) * per)
         kda.chunk_prefill(d["q"][s], d["k"][s], d["v"][s], d["g_raw"][s], d["b_raw"][s], d["A_log"],
                           d["dt_bias"], cu, pool, d["state_idx"], out[s], out_dtype=torch.float32,
                           workspace=ws)
+        states.append(pool.clone())
     torch.cuda.synchronize()
-    heads = [0, 19]
-    o_ref, p_ref, _ = oracle_run(inp, 32, 128, heads=heads)
-    assert rel_err(np64(out[:, heads]), o_ref[:, heads]) <= tol_for(torch.bfloat16, torch.float32)
-    assert rel_err(np64(pool[:, heads]), p_ref[:, heads]) <= tol_for(torch.bfloat16, torch.float32)
+    assert kda.check_device_errors() == 0
+    p = oracle.make_params(H, D)
+    ref_pool = inp["pool"]
+    slot = int(inp["state_idx"][0])
+    worst = [0.0, 0.0, 0.0, 0.0]                      # output, state; per head: output, state
+    tol = tol_for(torch.bfloat16, torch.float32)
+    for c in range(w.calls):
+        s = slice(c * per, (c + 1) * per)
+        o_ref, ref_pool, _ = oracle.forward(p, inp["q"][s], inp["k"][s], inp["v"][s], inp["g_raw"][s],
+                                            inp["b_raw"][s], inp["A_log"], inp["dt_bias"],
+                                            torch.tensor([0, per], dtype=torch.int32), ref_pool,
+                                            inp["state_idx"], nthreads=NTHREADS)
+        got_o = np64(out[s])
+        got_s = np64(states[c][slot:slot + 1])
+        e = (rel_err(got_o, o_ref), rel_err(got_s, ref_pool[slot:slot + 1]),
+             per_head_err(got_o, o_ref, [0, per]), per_head_err(got_s, ref_pool[slot:slot + 1]))
+        worst = [max(a, b) for a, b in zip(worst, e)]
+        assert e[0] <= tol and e[1] <= tol, (c, e)
+    print(f"long chunked prefill worst over 32 calls: output {worst[0]:.3e}, state {worst[1]:.3e}; "
+          f"per head: output {worst[2]:.3e}, state {worst[3]:.3e}")
+    assert worst[2] <= PER_HEAD_BF16 and worst[3] <= PER_HEAD_BF16, worst
 
 
 def test_prefill_then_decode_equals_one_prefill():

@@ -7,7 +7,9 @@ import torch
 
 import kda_gated_delta_gb300 as kda
 from kda_gated_delta_gb300 import workloads
-from helpers import np64, oracle_run, rel_err, tol_for
+import math
+
+from helpers import PER_HEAD_BF16, np64, oracle_run, per_head_err, rel_err, tol_for
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -61,6 +63,29 @@ def test_decode_full_workload():
     assert rel_err(np64(pool), p_ref) <= tol_for(torch.bfloat16, torch.float32)
     out32, pool32 = run_decode(inp, out_dtype=torch.float32)
     assert rel_err(np64(out32), o_ref) <= tol_for(torch.bfloat16, torch.float32)
+    # per (request, head), each normalised by its own largest reference value
+    used = inp["state_idx"].long()
+    e_oh = per_head_err(np64(out32), o_ref, inp["cu_seqlens"].tolist())
+    e_sh = per_head_err(np64(pool32)[used], p_ref[used])
+    print(f"decode per-head worst: output {e_oh:.3e}, state {e_sh:.3e}")
+    assert e_oh <= PER_HEAD_BF16 and e_sh <= PER_HEAD_BF16, (e_oh, e_sh)
+
+
+@pytest.mark.parametrize("gate,io", [("kda", torch.bfloat16), ("kda", torch.float32), ("gdn", torch.bfloat16)])
+def test_decode_softplus_threshold(gate, io):
+    """g_raw + dt_bias mostly above the softplus threshold of 20 (some below), with small rates
+    (A_log ~ U(ln 0.005, ln 0.05)) so that the decays stay moderate."""
+    H, D, B = 4, 128, 12
+    inp = workloads.make_inputs([1] * B, H, D, io, gate=gate, pool_slots=16, pool_std=0.3, seed=21,
+                                g_mean=21.0, g_std=3.0, dt_bias_std=1.0,
+                                A_log_range=(math.log(0.005), math.log(0.05)))
+    x = inp["g_raw"] + (inp["dt_bias"][None] if gate == "kda" else inp["dt_bias"][None, :])
+    assert (x > 20).float().mean() > 0.5 and (x <= 20).any()
+    out, pool = run_decode(inp, gate=gate)
+    o_ref, p_ref, _ = oracle_run(inp, H, D, gate=gate)
+    tol = tol_for(io, torch.float32)
+    assert rel_err(np64(out), o_ref) <= tol
+    assert rel_err(np64(pool), p_ref) <= tol
 
 
 def test_decode_out_of_range_slot_is_recorded():
@@ -109,7 +134,11 @@ def test_verify_full_workload_gdn():
     out, inter = run_verify(inp, 4, "gdn", out_dtype=torch.bfloat16)
     o_ref, _, i_ref = oracle_run(inp, 32, 128, gate="gdn", inter=True)
     assert rel_err(np64(out), o_ref) <= tol_for(torch.bfloat16, torch.bfloat16)
-    assert rel_err(np64(inter).reshape(256, 32, 128, 128), i_ref) <= tol_for(torch.bfloat16, torch.float32)
+    inter_np = np64(inter).reshape(256, 32, 128, 128)
+    assert rel_err(inter_np, i_ref) <= tol_for(torch.bfloat16, torch.float32)
+    e_sh = per_head_err(inter_np, i_ref)                    # per (token, head) intermediate state
+    print(f"verify per-head worst intermediate state: {e_sh:.3e}")
+    assert e_sh <= PER_HEAD_BF16, e_sh
 
 
 @pytest.mark.parametrize("gate", ["gdn", "kda"])
