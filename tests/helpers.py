@@ -18,7 +18,7 @@ TOL_BF16 = 2e-3
 TOL_BF16_OUT = 2e-3 + 2.0 ** -8
 # Per (sequence, head) error of the bf16-input workloads, each block normalised by its own
 # largest reference value (a stricter reading than the tensor-wide metric).
-PER_HEAD_BF16 = 4e-3
+PER_HEAD_BF16 = 2e-3
 
 
 def rel_err(gpu, ref) -> float:
