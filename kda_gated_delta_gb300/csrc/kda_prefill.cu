@@ -16,7 +16,7 @@
 //   state-pass kernel    the serial pass over a sequence's chunks, keeping S on chip.
 // bf16 inputs at C = 64, D = 128 take the tensor-core pair (chunk_intra_tc_kernel, two CTAs per SM,
 // and chunk_state_tc_kernel, one CTA per (sequence, head)), which exchange a per-(chunk, head)
-// record laid out as the state pass's shared-memory operand images (TcRec).  Every other shape and
+// record laid out as the state pass's shared-memory operand images (HRec).  Every other shape and
 // fp32 inputs take the fp32 CUDA-core pair (chunk_intra_kernel; chunk_state_kernel with one CTA
 // per (sequence, head, value tile)), which meets the 1e-5 bound of fp32 I/O.
 //
@@ -47,23 +47,24 @@ __device__ __forceinline__ void record_error(int32_t code) { atomicCAS(&g_prefil
 
 constexpr int kSub = 16;  // sub-block length of the decay split
 
-// Record of one (chunk, head) for the tensor-core state pass (C = 64, D = 128), in bytes.  It is
-// also the shared-memory image of that pass: operand images in the no-swizzle K-major layout of
-// kda_tc.cuh, already rounded to tf32.
-struct TcRec {
+// Record of one (chunk, head) for the tensor-core state pass (C = 64, D = 128), in bytes.  Its
+// parts are the shared-memory operand images of that pass, in fp16, in the no-swizzle layouts of
+// kda_tc.cuh (core matrices of 8 x 8 fp16; the 64-wide images are [row/8][k/8][row%8][k%8]):
+struct HRec {
     static constexpr int C = 64, D = 128;
-    static constexpr uint32_t W = 0;          // W:      rows r (64), K = c (128)  image
-    static constexpr uint32_t KT = 32768;     // Ktil^T: rows c (128), K = r (64)  image
-    static constexpr uint32_t U = 65536;      // U [r][v] fp32 (not rounded)
-    static constexpr uint32_t GL = 98304;     // e^{G_L} [c] fp32, 128 values + padding
-    static constexpr uint32_t QB = 98816;     // Qbar:   rows r (64), K = c (128)  image
-    static constexpr uint32_t P = 131584;     // P:      rows r (64), K = j (64)   image
-    static constexpr uint32_t BYTES = 147968;
+    static constexpr uint32_t W = 0;        // W: MN-major (N = r, K = c): [c/8][r/8][c%8][r%8]
+    static constexpr uint32_t KT = 16384;   // Ktil^T: K-major rows c, K = r: the same bytes as W's layout
+    static constexpr uint32_t QB = 32768;   // Qbar: K-major rows r, K = c: [r/8][c/8][r%8][c%8]
+    static constexpr uint32_t P = 49152;    // P: MN-major (N = r, K = j): [j/8][r/8][j%8][r%8]
+    static constexpr uint32_t U = 57344;    // U: [r/8][v][r%8]
+    static constexpr uint32_t GL = 73728;   // e^{G_L}[c], fp32
+    static constexpr uint32_t BYTES = 74240;
 };
 
 // ---- workspace layout ----------------------------------------------------------------------
 // [chunk table: 3 * max_chunks + (N + 1) + N int32, padded to 256 B]
-// [per (chunk, head): W C*D | Qbar C*D | Ktil C*D | U C*D | P C*C | gL D  floats, padded to 64]
+// [per (chunk, head) record: the fp16 HRec (tensor-core pair), or for the fp32 pair
+//  W C*D | Qbar C*D | Ktil C*D | U C*D | P C*C | gL D  floats, padded to 64]
 struct WsLayout {
     int64_t max_chunks;
     size_t table_bytes;
@@ -73,12 +74,13 @@ struct WsLayout {
 
 __host__ __device__ inline size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
 
-WsLayout ws_layout(int C, int D, int H, int32_t N, int64_t T)
+// tc: the tensor-core pair (bf16 inputs at C = 64, D = 128) and its fp16 record
+WsLayout ws_layout(int C, int D, int H, int32_t N, int64_t T, bool tc)
 {
     WsLayout w;
     w.max_chunks = (T + C - 1) / C + N;
     w.table_bytes = round_up(sizeof(int32_t) * (size_t)(3 * w.max_chunks + 2 * (int64_t)N + 1), 256);
-    w.per_chunk_head = round_up((size_t)4 * C * D + (size_t)C * C + D, 64);
+    w.per_chunk_head = tc ? HRec::BYTES / sizeof(float) : round_up((size_t)4 * C * D + (size_t)C * C + D, 64);
     w.total_bytes = w.table_bytes + sizeof(float) * w.per_chunk_head * (size_t)w.max_chunks * H;
     return w;
 }
@@ -234,10 +236,8 @@ struct IntraShape {
     static constexpr size_t BYTES = FLOATS * sizeof(float);
 };
 
-// Record written per (chunk, head).  TCREC = false: plain fp32 arrays for the SIMT state pass.
-// TCREC = true (C = 64, D = 128): the shared-memory image the tensor-core state pass copies in
-// one piece (see TcRec): tf32-rounded K-major operand images plus plain U and e^{G_L}.
-template <int C, int D, typename TIn, bool TCREC>
+// Record written per (chunk, head): plain fp32 arrays for the fp32 state pass.
+template <int C, int D, typename TIn>
 __global__ void __launch_bounds__(IntraShape<C, D>::THREADS, 1) chunk_intra_kernel(const IntraArgs a)
 {
     using Sh = IntraShape<C, D>;
@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(IntraShape<C, D>::THREADS, 1) chunk_intra_kern
     __syncthreads();
 
     float* rec = a.ws + ((size_t)ch * H + h) * a.ws_stride;
-    if constexpr (!TCREC) {
+    {
         float* wW = rec;
         float* wQ = rec + (size_t)C * D;
         float* wK = rec + (size_t)2 * C * D;
@@ -452,57 +452,6 @@ __global__ void __launch_bounds__(IntraShape<C, D>::THREADS, 1) chunk_intra_kern
             wK[e] = s_koT[c * PADC + r] * ea;
         }
         for (int e = tid; e < C * C; e += THREADS) wP[e] = s_P[(e / C) * PADC + (e % C)];
-        for (int c = tid; c < D; c += THREADS) {
-            float g = 1.f;
-            for (int bb = 0; bb < NB; ++bb) g *= s_bp[bb * D + c];
-            wG[c] = g;
-        }
-    } else {
-        static_assert(C == TcRec::C && D == TcRec::D, "tensor-core record shape");
-        float* wW = rec + TcRec::W / 4;
-        float* wK = rec + TcRec::KT / 4;
-        float* wU = rec + TcRec::U / 4;
-        float* wG = rec + TcRec::GL / 4;
-        float* wQ = rec + TcRec::QB / 4;
-        float* wP = rec + TcRec::P / 4;
-        // 6. forward substitution as above; U plain [r][v], W as a tf32 image (rows r, K = c)
-        if (tid < 2 * D) {
-            const bool isU = tid < D;
-            const int c = isU ? tid : tid - D;
-            float x[C];
-#pragma unroll
-            for (int r = 0; r < C; ++r) {
-                float rhs;
-                if (isU) {
-                    rhs = r < L ? s_beta[r] * to_f32(vp[((size_t)(t0 + r) * H + h) * D + c]) : 0.f;
-                } else {
-                    float eb = 1.f;
-                    for (int bb = 0; bb < r / kSub; ++bb) eb *= s_bp[bb * D + c];
-                    rhs = s_beta[r] * s_k[r * D + c] * eb;
-                }
-#pragma unroll
-                for (int jj = 0; jj < r; ++jj) rhs = fmaf(-s_A[r * PADC + jj], x[jj], rhs);
-                x[r] = rhs;
-                if (isU)
-                    wU[(size_t)r * D + c] = rhs;
-                else
-                    wW[tc::img_index(r, c, D)] = tc::round_tf32(rhs);
-            }
-        }
-        // 7. Qbar image (rows r, K = c), Ktil^T image (rows c, K = r), P image (rows r, K = j), e^{G_L}
-        for (int e = tid; e < C * D; e += THREADS) {
-            const int r = e / D, c = e % D;
-            const int blk = r / kSub;
-            float eb = 1.f, ea = 1.f;
-            for (int bb = 0; bb < blk; ++bb) eb *= s_bp[bb * D + c];
-            for (int bb = blk + 1; bb < NB; ++bb) ea *= s_bp[bb * D + c];
-            wQ[tc::img_index(r, c, D)] = tc::round_tf32(s_q[e] * eb);
-            wK[tc::img_index(c, r, C)] = tc::round_tf32(s_koT[c * PADC + r] * ea);
-        }
-        for (int e = tid; e < C * C; e += THREADS) {
-            const int r = e / C, j = e % C;
-            wP[tc::img_index(r, j, C)] = tc::round_tf32(s_P[r * PADC + j]);
-        }
         for (int c = tid; c < D; c += THREADS) {
             float g = 1.f;
             for (int bb = 0; bb < NB; ++bb) g *= s_bp[bb * D + c];
@@ -699,93 +648,93 @@ __global__ void __launch_bounds__(256, 1) chunk_state_kernel(const StateArgs a)
     }
 }
 
-// ---- inter-chunk state pass on the tensor cores (C = 64, D = 128) --------------------------------
-// One CTA of 384 threads per (sequence, head), in the transposed ("value-major") form so that every
-// MMA has M = 128 rows = the 128 value rows (TMEM lane v).  Per chunk:
-//   (a)  Dd   = S^T W^T                  A = tf32 copy of S^T in TMEM, B = W image       (N = 64)
-//   Delta^T = U^T - Dd, rounded to tf32, written over Dd
-//   (c)  Dc   = Delta^T Ktil             A = Delta^T in TMEM,          B = Ktil^T image  (N = 128)
-//   S^T <- S^T Diag(e^{G_L}) + Dc (fp32 in registers), its tf32 copy into the other TMEM buffer
-//   (b2) Do   = Delta^T P^T              A = Delta^T,                  B = P image       (N = 64)
-//   (b)  Do  += S^T Qbar^T               A = S^T (this chunk's copy),  B = Qbar image    (N = 64)
-//   O^T = Do -> out
-// Warps 0..7 share the chain: thread v of warp group g (0: warps 0..3, 1: warps 4..7) is TMEM
-// lane v and owns columns 64 g .. 64 g + 63 of row v of S^T in registers; each group computes half
-// of Delta (rows r = 32 g ..) and half of the S update.  Thread 0 issues (a) and (c) and loads W,
-// U/gL and Ktil^T.  Warps 8..11 produce the output: thread 256 issues (b2) and (b) once Delta is
-// ready and P / Qbar have landed, and loads P and Qbar; the four warps copy Do to the output.
-// Neither the output MMAs, their operands nor the output stores sit on the chain.  The S^T copy is
-// double-buffered (chunk i reads buffer i & 1), so the S update of chunk i only waits for (b) of
-// chunk i - 1.  Hand-offs are mbarriers (delta_ready: an arrival of thread 0; b2_done,
-// out_ready[2]: tensor-core commits of thread 256).  Operand images arrive by bulk async copy from
-// the record: W and U/gL double-buffered (two chunks ahead), Ktil^T, P and Qbar one chunk ahead.
-// All waits are bounded and give up early once any thread has recorded a failure; loop exits are
-// made uniform with barrier reductions.
+// ---- inter-chunk state pass on the tensor cores (C = 64, D = 128, fp16 operands) -----------------
+// One CTA per (sequence, head), in the transposed ("value-major") form: TMEM lane v holds value row
+// v, so every chain MMA has M = 128.  Per chunk i of the sequence, with the record's W_i, Ktil_i, U_i,
+// Qbar_i, P_i and gamma_i = e^{G_L} of chunk i:
+//   Delta_i  = U_i - S_i W_i^T                      (value-major: Delta_i^T[v][r])
+//   O_i      = Qbar_i S_i + P_i Delta_i
+//   S_{i+1}  = Diag(gamma_i) S_i + Ktil_i^T Delta_i
+// Substituting the last line into the first one of the next chunk gives the chain one MMA per chunk:
+//   Delta_{i+1} = U_{i+1} - (W_{i+1} Diag(gamma_i)) S_i - (W_{i+1} Ktil_i^T) Delta_i,
+// whose second operands W'_{i+1} = W_{i+1} Diag(gamma_i) and Z_{i+1} = W_{i+1} Ktil_i^T depend on
+// record data only and are prepared ahead, off the chain.  S_{i+1} (needed as an operand one
+// chunk later) and the output are computed beside the chain.  Roles (18 warps):
+//   warps 0..3    Delta pass: Delta_i^T = U_i^T - (chain accumulator), rounded to fp16, into TMEM
+//   warps 4..11   S update (fp32 in registers, two groups of 64 key columns) and its fp16 copy
+//   warps 12..15  Z epilogue (Z_j accumulator -> fp16 operand image), W'_j scaling, output copy
+//   warp 16       issues the chain MMA and (c) = Delta^T Ktil, and the record copies W, Ktil, U
+//   warp 17       issues Z_j and the output MMAs, and the Qbar / P copies
+// Operands in TMEM (fp16 pairs): S^T (two buffers), Delta^T (two buffers); accumulators (fp32): the
+// chain, (c), the output and Z.  Operand images arrive by bulk copy straight from the record.
+// Hand-offs are mbarriers: MMA completions by tcgen05.commit, the passes by thread arrivals.  Every
+// wait is bounded and gives up early once any thread has recorded a failure; a role that gives up
+// leaves its loop, the issuers let their MMAs and copies land (bounded), and the slot is left as it
+// was.  No named barrier is used inside the loops, so roles can leave them at different points.
 constexpr uint32_t kWaitPolls = 1u << 24;
 
-// shared memory: the record image (one buffer set) followed by the second W and U/gL buffers
-constexpr uint32_t kSmW1 = TcRec::BYTES;
-constexpr uint32_t kSmUG1 = kSmW1 + 32768;
-constexpr uint32_t kUGBytes = 32768 + 512;
-constexpr uint32_t kSmBars = kSmUG1 + kUGBytes;
-struct TcBars {
-    uint64_t w[2], ug[2], kt, qb, p;  // operand buffers filled (tx bytes); these seven come first
-    uint64_t mma_a;                   // (a) complete                    (thread 0 commit)
-    uint64_t mma_c;                   // (c) complete                    (thread 0 commit)
-    uint64_t delta_ready;             // Delta^T of the chunk is in TMEM (thread 0 arrives)
-    uint64_t b2_done;                 // (b2) complete: Delta^T may be overwritten (issuer commit)
-    uint64_t out_ready[2];            // (b) of chunk i complete, Do ready; index i & 1 (issuer commit)
-    uint64_t drain[2];                // used once each, to drain the tensor core after a failed wait
+namespace stc {
+constexpr uint32_t SM_W = 0;            // 4 x 16384: W_j, scaled in place to W'_j; slot j % 4
+constexpr uint32_t SM_KT = 65536;       // 4 x 16384: Ktil^T_j; slot j % 4
+constexpr uint32_t SM_U = 131072;       // 2 x 16384: U_j; slot j % 2
+constexpr uint32_t SM_QB = 163840;      // 16384: Qbar_j, followed by P_j (one copy)
+constexpr uint32_t SM_P = 180224;       // 8192
+constexpr uint32_t SM_Z = 188416;       // 2 x 8192: Z_j image; slot j % 2
+constexpr uint32_t SM_GL = 212992;      // 4 x 512: gamma_j, copied with Ktil^T_j; slot j % 4
+constexpr uint32_t SM_BAR = 215040;     // mbarriers
+constexpr uint32_t SM_MISC = SM_BAR + 256;
+constexpr uint32_t BYTES = SM_MISC + 64;
+constexpr int THREADS = 576;
+static_assert(SM_QB + 16384 == SM_P && SM_P + 8192 == SM_Z, "layout");
+static_assert(BYTES <= 232448, "state-pass shared memory");
+// TMEM columns (512 allocated; each accumulator starts at a multiple of its width)
+constexpr uint32_t T_SH = 0;     // fp16 S^T, two buffers (2 x 64 cols)
+constexpr uint32_t T_DH = 128;   // fp16 Delta^T, two buffers (2 x 32)
+constexpr uint32_t T_DA = 192;   // chain accumulator [v][r] (64)
+constexpr uint32_t T_DC = 256;   // (c) accumulator Delta^T Ktil [v][c] (128)
+constexpr uint32_t T_DO = 384;   // output accumulator O^T [v][r] (64)
+constexpr uint32_t T_DZ = 448;   // Z accumulator, M = 64: lane 32 (r' >> 4) + (r' & 15), columns r (64)
+}  // namespace stc
+
+struct StBars {
+    uint64_t w[4], kt[4], u[2], qp;   // record copies landed (tx bytes)
+    uint64_t chain;                   // chain MMA of chunk j complete        (warp 16 commit)
+    uint64_t c;                       // (c) of chunk j complete              (warp 16 commit)
+    uint64_t z;                       // Z_j complete                         (warp 17 commit)
+    uint64_t o[2];                    // outputs of chunk i complete, i & 1   (warp 17 commit)
+    uint64_t delta_ready[2];          // Delta_j in TMEM, index j & 1         (128 arrivals)
+    uint64_t sh_ready[2];             // S_j done (fp16 copy in TMEM), j & 1  (256 arrivals)
+    uint64_t zw_ready[2];             // Z_j image and W'_j ready, (j-1) & 1  (128 arrivals)
+    uint64_t dz_free;                 // Z accumulator read                   (128 arrivals)
+    uint64_t do_free;                 // output accumulator read              (128 arrivals)
+    uint64_t drain[2];                // each issuer's final completion wait
 };
-constexpr size_t kTcSmemBytes = kSmBars + 1024;
-static_assert(sizeof(TcBars) + 32 + 512 <= 1024, "barriers, TMEM base, abort flag and e^{G_L}");
-static_assert(kTcSmemBytes <= 232448, "state-pass shared memory");
-constexpr int kStateThreads = 384;
+static_assert(sizeof(StBars) <= 256, "barriers");
 
-// TMEM column map (512 columns allocated; each accumulator starts at a multiple of its width)
-constexpr uint32_t kT_SOP = 0;     // tf32 S^T, two buffers   (2 x 128 cols, A operand)
-constexpr uint32_t kT_SC = 256;    // Delta^T Ktil            (128, accumulator)
-constexpr uint32_t kT_DD = 384;    // S^T W^T, then Delta^T   (64, accumulator, then A operand)
-constexpr uint32_t kT_OUT = 448;   // O^T                     (64, accumulator)
-
-__device__ __forceinline__ void chain_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-// Named barrier that also returns, to every participating thread, whether any of them passed a
-// true flag: a loop exit after a failure is uniform even though the failure flag is written
-// asynchronously by other warps.  Barrier 1: the 256 chain threads; barrier 2: the 128 output threads.
-template <int ID, int COUNT>
-__device__ __forceinline__ bool sync_any(bool flag)
+// byte offset of element (row, k) in the 64-column fp16 images [row/8][k/8][row%8][k%8]
+// (K-major with 64 K columns, or MN-major with 64 M/N columns: the same bytes)
+__device__ __forceinline__ uint32_t h64(uint32_t row, uint32_t k)
 {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.or.pred po, %2, %3, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)flag), "n"(ID), "n"(COUNT)
-        : "memory");
-    return r != 0;
+    return (row >> 3) * 1024u + (k >> 3) * 128u + (row & 7u) * 16u + (k & 7u) * 2u;
 }
-__device__ __forceinline__ bool chain_sync_any(bool flag) { return sync_any<1, 256>(flag); }
-__device__ __forceinline__ bool output_sync_any(bool flag) { return sync_any<2, 128>(flag); }
 
 template <typename TOut>
-__global__ void __launch_bounds__(kStateThreads, 1) chunk_state_tc_kernel(const StateArgs a)
+__global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const StateArgs a)
 {
-    constexpr int C = TcRec::C, D = TcRec::D, DH = D / 2;
+    using namespace stc;
+    constexpr int C = HRec::C, D = HRec::D;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = smem_raw;
-    TcBars* bars = reinterpret_cast<TcBars*>(sm + kSmBars);
-    uint32_t* s_taddr = reinterpret_cast<uint32_t*>(sm + kSmBars + sizeof(TcBars));
-    volatile int* s_abort = reinterpret_cast<volatile int*>(sm + kSmBars + sizeof(TcBars) + 16);
-    float* s_gl = reinterpret_cast<float*>(sm + kSmBars + sizeof(TcBars) + 32);  // e^{G_L} of the chunk
+    StBars* bars = reinterpret_cast<StBars*>(sm + SM_BAR);
+    uint32_t* s_taddr = reinterpret_cast<uint32_t*>(sm + SM_MISC);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(sm + SM_MISC + 16);
 
     // longest sequences first: CTA x -> (rank, head), rank -> sequence through seq_order
     const int H = a.H;
     const int rank = blockIdx.x / H;
     const int h = blockIdx.x - rank * H;
     const int seq = a.seq_order[rank];
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     TOut* out = reinterpret_cast<TOut*>(a.out);
 
     int64_t slot = a.state_idx[seq];
@@ -804,14 +753,23 @@ __global__ void __launch_bounds__(kStateThreads, 1) chunk_state_tc_kernel(const 
         return;
     }
     if (c_begin >= c_end) return;  // empty sequence: the slot keeps its state
+    const int n = (int)(c_end - c_begin);
 
     if (warp == 0) {
         tc::tmem_alloc(s_taddr, 512);
         tc::tmem_relinquish();
     }
     if (tid == 0) {
-        uint64_t* b = reinterpret_cast<uint64_t*>(bars);
-        for (int i = 0; i < (int)(sizeof(TcBars) / 8); ++i) tc::mbar_init(b + i, 1);
+        for (int i = 0; i < 4; ++i) { tc::mbar_init(&bars->w[i], 1); tc::mbar_init(&bars->kt[i], 1); }
+        tc::mbar_init(&bars->u[0], 1); tc::mbar_init(&bars->u[1], 1); tc::mbar_init(&bars->qp, 1);
+        tc::mbar_init(&bars->chain, 1); tc::mbar_init(&bars->c, 1); tc::mbar_init(&bars->z, 1);
+        tc::mbar_init(&bars->o[0], 1); tc::mbar_init(&bars->o[1], 1);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&bars->delta_ready[i], 128); tc::mbar_init(&bars->sh_ready[i], 256);
+            tc::mbar_init(&bars->zw_ready[i], 128);
+        }
+        tc::mbar_init(&bars->dz_free, 128); tc::mbar_init(&bars->do_free, 128);
+        tc::mbar_init(&bars->drain[0], 1); tc::mbar_init(&bars->drain[1], 1);
         *s_abort = 0;
         tc::fence_mbar_init();
     }
@@ -819,7 +777,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) chunk_state_tc_kernel(const 
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *s_taddr;
-    const uint32_t lane = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
     // bounded wait that also gives up once any thread has recorded a failure
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -830,230 +788,295 @@ __global__ void __launch_bounds__(kStateThreads, 1) chunk_state_tc_kernel(const 
         *s_abort = 1;
         return false;
     };
-    auto rec_of = [&](int64_t ch) -> const unsigned char* {
-        return reinterpret_cast<const unsigned char*>(a.ws + ((size_t)ch * H + h) * a.ws_stride);
+    auto rec_of = [&](int j) -> const unsigned char* {
+        return reinterpret_cast<const unsigned char*>(a.ws + ((size_t)(c_begin + j) * H + h) * a.ws_stride);
     };
-    // copies in flight per load barrier (bookkeeping of the issuing thread, for the drain)
-    uint64_t* const bar0 = &bars->w[0];
-    uint32_t pend_mask = 0, pend_par = 0, uses[7] = {0, 0, 0, 0, 0, 0, 0};
-    auto load = [&](uint64_t* bar, uint32_t dst_off, uint32_t src_off, uint32_t bytes, int64_t ch) {
-        const uint32_t bi = (uint32_t)(bar - bar0), bit = 1u << bi;
-        pend_mask |= bit;
-        pend_par = (pend_par & ~bit) | ((uses[bi] & 1u) ? bit : 0u);
-        ++uses[bi];
-        tc::mbar_arrive_expect_tx(bar, bytes);
-        tc::bulk_g2s(sm + dst_off, rec_of(ch) + src_off, bytes, bar);
-    };
-    auto landed = [&](uint64_t* bar) { pend_mask &= ~(1u << (uint32_t)(bar - bar0)); };
-    auto drain = [&](uint64_t* dbar) {          // after a failure: own MMAs and copies land, bounded
-        tc::mma_commit(dbar);
-        tc::mbar_wait(dbar, 0, kWaitPolls);
-        for (uint32_t bi = 0; bi < 7; ++bi)
-            if (pend_mask & (1u << bi)) tc::mbar_wait(bar0 + bi, (pend_par >> bi) & 1u, kWaitPolls);
-    };
-    constexpr uint32_t kId64 = tc::idesc_tf32(128, 64), kId128 = tc::idesc_tf32(128, 128);
+    auto desc = [](const unsigned char* p, uint32_t lbo, uint32_t sbo) { return tc::smem_desc(tc::smem_u32(p), lbo, sbo); };
+    float S[D / 2];   // the S update threads: columns 64 g .. 64 g + 63 of row v of S^T (fp32)
 
-    if (warp >= 8) {
-        // ---- output side: thread 256 issues (b2) and (b); warps 8..11 copy Do to the output
-        const int v = tid - 256;
-        const bool issuer = (v == 0);
-        const uint32_t sQB = tc::smem_u32(sm + TcRec::QB), sP = tc::smem_u32(sm + TcRec::P);
-        if (issuer) {
-            load(&bars->p, TcRec::P, TcRec::P, 16384, c_begin);
-            load(&bars->qb, TcRec::QB, TcRec::QB, 32768, c_begin);
-        }
-        bool ok = true;
-        for (int64_t ch = c_begin; ch < c_end; ++ch) {
-            const uint32_t i = (uint32_t)(ch - c_begin), ph = i & 1u;
-            if (issuer) {
-                ok = wait(&bars->delta_ready, ph) && wait(&bars->p, ph);
+    if (warp >= 16) {
+        // ---- the two issuers (lane 0 of warps 16 and 17); copies in flight are tracked per barrier
+        if (lane == 0) {
+            uint64_t* const lbar0 = &bars->w[0];          // w[4], kt[4], u[2], qp: 11 load barriers
+            uint32_t uses[11] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+            auto issue = [&](uint64_t* bar, int j, uint32_t dst, uint32_t src, uint32_t bytes, uint32_t dst2,
+                             uint32_t src2, uint32_t bytes2) {
+                ++uses[bar - lbar0];
+                tc::mbar_arrive_expect_tx(bar, bytes + bytes2);
+                tc::bulk_g2s(sm + dst, rec_of(j) + src, bytes, bar);
+                if (bytes2) tc::bulk_g2s(sm + dst2, rec_of(j) + src2, bytes2, bar);
+            };
+            bool ok = true;
+            const int me = warp - 16;
+            if (me == 0) {
+                // ---- warp 16: chain MMA and (c); copies of W, Ktil^T + gamma, U
+                auto load_w = [&](int j) { issue(&bars->w[j & 3], j, SM_W + 16384u * (j & 3), HRec::W, 16384, 0, 0, 0); };
+                auto load_kt = [&](int j) {
+                    issue(&bars->kt[j & 3], j, SM_KT + 16384u * (j & 3), HRec::KT, 16384, SM_GL + 512u * (j & 3), HRec::GL, 512);
+                };
+                auto load_u = [&](int j) { issue(&bars->u[j & 1], j, SM_U + 16384u * (j & 1), HRec::U, 16384, 0, 0, 0); };
+                constexpr uint32_t idChainS = tc::idesc_f16(128, 64, false, true);   // B = W' (MN-major)
+                constexpr uint32_t idChainZ = tc::idesc_f16(128, 64);                // B = Z (K-major)
+                constexpr uint32_t idC = tc::idesc_f16(128, 128);                    // B = Ktil^T (K-major)
+                for (int j = 0; j < 4 && j < n; ++j) load_w(j);
+                for (int j = 0; j < 3 && j < n; ++j) load_kt(j);
+                for (int j = 0; j < 2 && j < n; ++j) load_u(j);
+                // chain MMA of chunk 0: S_0 W_0^T
+                ok = wait(&bars->sh_ready[0], 0) && wait(&bars->w[0], 0);
                 if (ok) {
-                    landed(&bars->p);
                     tc::tc_fence_after();
 #pragma unroll
-                    for (int s = 0; s < C / 8; ++s)
-                        tc::mma_tf32_ts(tmem + kT_OUT, tmem + kT_DD + 8 * s, tc::smem_desc(sP + 256 * s, 128, 2048), kId64, s > 0);
-                    tc::mma_commit(&bars->b2_done);
-                    ok = wait(&bars->qb, ph);
+                    for (int s = 0; s < D / 16; ++s)
+                        tc::mma_f16_ts(tmem + T_DA, tmem + T_SH + 8 * s, desc(sm + SM_W + 2048 * s, 1024, 128), idChainS, s > 0);
+                    tc::mma_commit(&bars->chain);
                 }
-                if (ok) {
-                    landed(&bars->qb);
+                for (int i = 0; ok && i < n; ++i) {
+                    // Delta_i is in TMEM; S_i is done (so the update pass is done reading (c) of i - 1)
+                    if (!(ok = wait(&bars->delta_ready[i & 1], (i >> 1) & 1) && wait(&bars->sh_ready[i & 1], (i >> 1) & 1)))
+                        break;
+                    if (i + 1 < n) {   // chain MMA of chunk i + 1: S_i W'^T_{i+1} + Delta_i Z^T_{i+1}
+                        if (!(ok = wait(&bars->zw_ready[i & 1], (i >> 1) & 1))) break;
+                        tc::tc_fence_after();
+                        const uint32_t sh = tmem + T_SH + 64 * (i & 1), dh = tmem + T_DH + 32 * (i & 1);
+                        const unsigned char* wb = sm + SM_W + 16384u * ((i + 1) & 3);
+                        const unsigned char* zb = sm + SM_Z + 8192u * ((i + 1) & 1);
 #pragma unroll
-                    for (int s = 0; s < D / 8; ++s)
-                        tc::mma_tf32_ts(tmem + kT_OUT, tmem + kT_SOP + 128 * (i & 1u) + 8 * s,
-                                        tc::smem_desc(sQB + 256 * s, 128, 4096), kId64, 1);
-                    tc::mma_commit(&bars->out_ready[i & 1u]);
+                        for (int s = 0; s < D / 16; ++s)
+                            tc::mma_f16_ts(tmem + T_DA, sh + 8 * s, desc(wb + 2048 * s, 1024, 128), idChainS, s > 0);
+#pragma unroll
+                        for (int s = 0; s < C / 16; ++s)
+                            tc::mma_f16_ts(tmem + T_DA, dh + 8 * s, desc(zb + 256 * s, 128, 1024), idChainZ, 1);
+                        tc::mma_commit(&bars->chain);
+                    }
+                    // (c): Delta_i^T Ktil_i
+                    if (!(ok = wait(&bars->kt[i & 3], (i >> 2) & 1))) break;
+                    tc::tc_fence_after();
+                    {
+                        const uint32_t dh = tmem + T_DH + 32 * (i & 1);
+                        const unsigned char* kb = sm + SM_KT + 16384u * (i & 3);
+#pragma unroll
+                        for (int s = 0; s < C / 16; ++s)
+                            tc::mma_f16_ts(tmem + T_DC, dh + 8 * s, desc(kb + 256 * s, 128, 1024), idC, s > 0);
+                        tc::mma_commit(&bars->c);
+                    }
+                    // slots freed this step: W_i (its chain MMA is done), U_i (read by the Delta pass),
+                    // Ktil_{i-1} and gamma_{i-1} (their last readers signalled sh_ready(i) / zw_ready(i))
+                    if (i + 4 < n) load_w(i + 4);
+                    if (i + 3 < n) load_kt(i + 3);
+                    if (i + 2 < n) load_u(i + 2);
+                }
+            } else {
+                // ---- warp 17: Z_j = W_j Ktil_{j-1}^T and the outputs; copies of Qbar + P
+                auto load_qp = [&](int j) { issue(&bars->qp, j, SM_QB, HRec::QB, 24576, 0, 0, 0); };
+                constexpr uint32_t idZ = tc::idesc_f16(64, 64, true, true);    // A = W, B = Ktil (both MN-major)
+                constexpr uint32_t idB2 = tc::idesc_f16(128, 64, false, true); // B = P (MN-major)
+                constexpr uint32_t idB = tc::idesc_f16(128, 64);               // B = Qbar (K-major)
+                auto issue_z = [&](int m) -> bool {
+                    if (!(wait(&bars->w[m & 3], (m >> 2) & 1) && wait(&bars->kt[(m - 1) & 3], ((m - 1) >> 2) & 1) &&
+                          (m == 1 || wait(&bars->dz_free, (m - 2) & 1))))
+                        return false;
+                    tc::tc_fence_after();
+                    const unsigned char* wb = sm + SM_W + 16384u * (m & 3);
+                    const unsigned char* kb = sm + SM_KT + 16384u * ((m - 1) & 3);
+#pragma unroll
+                    for (int s = 0; s < D / 16; ++s)
+                        tc::mma_f16_ss(tmem + T_DZ, desc(wb + 2048 * s, 1024, 128), desc(kb + 2048 * s, 1024, 128), idZ, s > 0);
+                    tc::mma_commit(&bars->z);
+                    return true;
+                };
+                load_qp(0);
+                ok = n < 2 || issue_z(1);
+                for (int i = 0; ok && i < n; ++i) {
+                    if (i + 2 < n && !(ok = issue_z(i + 2))) break;
+                    if (!(ok = wait(&bars->delta_ready[i & 1], (i >> 1) & 1) && wait(&bars->sh_ready[i & 1], (i >> 1) & 1) &&
+                               wait(&bars->qp, i & 1) &&
+                               (i == 0 || wait(&bars->do_free, (i - 1) & 1))))
+                        break;
+                    tc::tc_fence_after();
+                    const uint32_t sh = tmem + T_SH + 64 * (i & 1), dh = tmem + T_DH + 32 * (i & 1);
+#pragma unroll
+                    for (int s = 0; s < C / 16; ++s)   // (b2) P_i Delta_i
+                        tc::mma_f16_ts(tmem + T_DO, dh + 8 * s, desc(sm + SM_P + 2048 * s, 1024, 128), idB2, s > 0);
+#pragma unroll
+                    for (int s = 0; s < D / 16; ++s)   // (b) + Qbar_i S_i
+                        tc::mma_f16_ts(tmem + T_DO, sh + 8 * s, desc(sm + SM_QB + 256 * s, 128, 2048), idB, 1);
+                    tc::mma_commit(&bars->o[i & 1]);
+                    if (i + 1 < n) {   // Qbar and P are free once the outputs are done
+                        if (!(ok = wait(&bars->o[i & 1], (i >> 1) & 1))) break;
+                        load_qp(i + 1);
+                    }
                 }
             }
-            const bool okr = ok && wait(&bars->out_ready[i & 1u], (i >> 1) & 1u);   // every output thread
-            if (okr) {
-                tc::tc_fence_after();
-                if (issuer && ch + 1 < c_end) {          // (b2) and (b) are done with P and Qbar
-                    load(&bars->p, TcRec::P, TcRec::P, 16384, ch + 1);
-                    load(&bars->qb, TcRec::QB, TcRec::QB, 32768, ch + 1);
-                }
-                const int64_t t0 = a.chunk_start[ch];
-                const int L = a.chunk_len[ch];
-#pragma unroll
-                for (int r0 = 0; r0 < C; r0 += 16) {
-                    float o[16];
-                    tc::tmem_ld16(tmem + lane + kT_OUT + r0, o);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (r0 + j < L) out[((size_t)(t0 + r0 + j) * H + h) * D + v] = from_f32<TOut>(o[j]);
-                }
-            }
-            tc::tc_fence_before();
-            if (output_sync_any(!okr || *s_abort != 0)) break;   // Do is free for the next (b2)
+            // let this issuer's MMAs and copies land before the CTA exits (bounded)
+            tc::mma_commit(&bars->drain[me]);
+            tc::mbar_wait(&bars->drain[me], 0, kWaitPolls);
+            for (int bi = 0; bi < 11; ++bi)
+                if (uses[bi]) tc::mbar_wait(lbar0 + bi, (uses[bi] - 1) & 1u, kWaitPolls);
+            if (!ok) *s_abort = 1;
         }
-        if (issuer && *s_abort) drain(&bars->drain[1]);
         __syncwarp();
-    } else {
-        // ---- the chain: warp group g = warp >> 2 owns S^T columns 64 g .. 64 g + 63 of row v
-        const int g = warp >> 2, v = tid & (D - 1);
-        auto w_off = [](uint32_t b) { return b ? kSmW1 : TcRec::W; };
-        auto ug_off = [](uint32_t b) { return b ? kSmUG1 : TcRec::U; };
-        if (tid == 0) {
-            load(&bars->w[0], TcRec::W, TcRec::W, 32768, c_begin);
-            load(&bars->ug[0], TcRec::U, TcRec::U, kUGBytes, c_begin);
-            load(&bars->kt, TcRec::KT, TcRec::KT, 32768, c_begin);
-            if (c_begin + 1 < c_end) {
-                load(&bars->w[1], kSmW1, TcRec::W, 32768, c_begin + 1);
-                load(&bars->ug[1], kSmUG1, TcRec::U, kUGBytes, c_begin + 1);
-            }
-        }
-
-        // entry state: columns 64 g .. of row v of S^T = pool[slot][h][v][:]; tf32 copy -> buffer 0
-        float S[DH];
-        const float* Sg = a.pool + ((size_t)slot * H + h) * (size_t)D * D + (size_t)v * D + DH * g;
+    } else if (warp < 4) {
+        // ---- Delta pass: Delta_j^T[v][r] = U_j[r][v] - chain[v][r], fp16 into TMEM buffer j & 1
+        const int v = tid;
+        for (int j = 0; j < n; ++j) {
+            bool okw = wait(&bars->chain, j & 1) && (j < 2 || wait(&bars->o[j & 1], ((j - 2) >> 1) & 1)) &&
+                       wait(&bars->u[j & 1], (j >> 1) & 1);
+            if (!__all_sync(0xffffffffu, okw)) break;
+            tc::tc_fence_after();
+            const unsigned char* ub = sm + SM_U + 16384u * (j & 1);
+            const uint32_t dst = tmem + lane_base + T_DH + 32 * (j & 1);
 #pragma unroll
-        for (int c = 0; c < DH; c += 4) {
+            for (int r0 = 0; r0 < C; r0 += 16) {
+                float d[16];
+                tc::tmem_ld16(tmem + lane_base + T_DA + r0, d);
+                const uint4 u0 = *reinterpret_cast<const uint4*>(ub + ((((r0 >> 3) + 0) * 128 + v) << 4));
+                const uint4 u1 = *reinterpret_cast<const uint4*>(ub + ((((r0 >> 3) + 1) * 128 + v) << 4));
+                const uint32_t uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                uint32_t pk[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    float lo, hi;
+                    tc::unpack_f16x2(uu[t], lo, hi);
+                    pk[t] = tc::pack_f16x2(lo - d[2 * t], hi - d[2 * t + 1]);
+                }
+                tc::tmem_st8u_nowait(dst + r0 / 2, pk);
+            }
+            tc::tmem_wait_st();
+            tc::tc_fence_before();
+            tc::mbar_arrive(&bars->delta_ready[j & 1]);
+        }
+    } else if (warp < 12) {
+        // ---- S update: S_{j+1} = Diag(gamma_j) S_j + (c), on key columns 64 g .. 64 g + 63 of row v
+        const int g = (warp - 4) >> 2, v = tid & (D - 1);
+        const float* Sg = a.pool + ((size_t)slot * H + h) * (size_t)D * D + (size_t)v * D + 64 * g;
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
             const float4 x = *reinterpret_cast<const float4*>(Sg + c);
             S[c] = x.x; S[c + 1] = x.y; S[c + 2] = x.z; S[c + 3] = x.w;
         }
 #pragma unroll
-        for (int c = 0; c < DH; c += 16) {
-            float t[16];
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+            uint32_t pk[8];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) t[j] = tc::round_tf32(S[c + j]);
-            tc::tmem_st16_nowait(tmem + lane + kT_SOP + DH * g + c, t);
+            for (int t = 0; t < 8; ++t) pk[t] = tc::pack_f16x2(S[c0 + 2 * t], S[c0 + 2 * t + 1]);
+            tc::tmem_st8u_nowait(tmem + lane_base + T_SH + 32 * g + c0 / 2, pk);
         }
         tc::tmem_wait_st();
         tc::tc_fence_before();
-        chain_sync();
-
-        const uint32_t sKT = tc::smem_u32(sm + TcRec::KT);
-        bool ok = true;
-        for (int64_t ch = c_begin; ch < c_end; ++ch) {
-            const uint32_t i = (uint32_t)(ch - c_begin);
-            const uint32_t ph = i & 1u, b = i & 1u, phb = (i >> 1) & 1u;
-            const float* sU = reinterpret_cast<const float*>(sm + ug_off(b));
-            const float* sG = sU + 32768 / 4;
-
-            // (a): Dd is the previous chunk's Delta^T, free once its (b2) is done
-            if (tid == 0) {
-                tc::tc_fence_after();
-                ok = wait(&bars->w[b], phb) && (i == 0 || wait(&bars->b2_done, (i - 1) & 1u)) && ok;
-                if (ok) {
-                    landed(&bars->w[b]);
-                    tc::tc_fence_after();
-                    const uint32_t sW = tc::smem_u32(sm + w_off(b));
+        tc::mbar_arrive(&bars->sh_ready[0]);
+        for (int j = 0; j < n; ++j) {
+            bool okw = wait(&bars->c, j & 1) && wait(&bars->kt[j & 3], (j >> 2) & 1) &&
+                       (j < 1 || wait(&bars->o[(j - 1) & 1], ((j - 1) >> 1) & 1));
+            if (!__all_sync(0xffffffffu, okw)) break;
+            tc::tc_fence_after();
+            const float* gl = reinterpret_cast<const float*>(sm + SM_GL + 512u * (j & 3)) + 64 * g;
+            const uint32_t dst = tmem + lane_base + T_SH + 64 * ((j + 1) & 1) + 32 * g;
+            const bool more = j + 1 < n;
 #pragma unroll
-                    for (int s = 0; s < D / 8; ++s)
-                        tc::mma_tf32_ts(tmem + kT_DD, tmem + kT_SOP + 128 * b + 8 * s, tc::smem_desc(sW + 256 * s, 128, 4096),
-                                        kId64, s > 0);
-                    tc::mma_commit(&bars->mma_a);
+            for (int c0 = 0; c0 < 64; c0 += 16) {
+                float d[16];
+                tc::tmem_ld16(tmem + lane_base + T_DC + 64 * g + c0, d);
+#pragma unroll
+                for (int t = 0; t < 16; ++t) S[c0 + t] = fmaf(S[c0 + t], gl[c0 + t], d[t]);
+                if (more) {
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) pk[t] = tc::pack_f16x2(S[c0 + 2 * t], S[c0 + 2 * t + 1]);
+                    tc::tmem_st8u_nowait(dst + c0 / 2, pk);
                 }
             }
-            // Delta^T = U^T - S^T W^T (rows r = 32 g .. 32 g + 31), rounded, over Dd
-            {
-                const bool okw = wait(&bars->ug[b], phb) && wait(&bars->mma_a, ph);
-                if (okw && tid == 0) landed(&bars->ug[b]);
-                tc::tc_fence_after();
-                if (okw) {
+            if (more) tc::tmem_wait_st();
+            if (a.snap) {                                // state after this chunk
+                const int64_t ch = c_begin + j;
+                if (ch < a.snap_cap) {
+                    float* Sd = a.snap + (((size_t)ch * H + h) * D + v) * (size_t)D + 64 * g;
 #pragma unroll
-                    for (int r0 = 32 * g; r0 < 32 * g + 32; r0 += 16) {
-                        float d[16];
-                        tc::tmem_ld16(tmem + lane + kT_DD + r0, d);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) d[j] = tc::round_tf32(sU[(r0 + j) * D + v] - d[j]);
-                        tc::tmem_st16_nowait(tmem + lane + kT_DD + r0, d);
-                    }
-                    if (g == 0) s_gl[v] = sG[v];         // the buffer is refilled before (c) retires
-                    tc::tmem_wait_st();
+                    for (int c = 0; c < 64; c += 4) *reinterpret_cast<float4*>(Sd + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+                } else if (v == 0 && g == 0) {
+                    record_error(kDevErrSeqlens);
                 }
             }
             tc::tc_fence_before();
-            if (chain_sync_any(*s_abort != 0)) break;
-            if (tid == 0) {                              // Delta ready; refill W, U/gL(b); (c)
-                tc::tc_fence_after();
-                tc::mbar_arrive(&bars->delta_ready);
-                if (ch + 2 < c_end) {
-                    load(&bars->w[b], w_off(b), TcRec::W, 32768, ch + 2);
-                    load(&bars->ug[b], ug_off(b), TcRec::U, kUGBytes, ch + 2);
-                }
-                ok = wait(&bars->kt, ph) && ok;
-                if (ok) {
-                    landed(&bars->kt);
-                    tc::tc_fence_after();
+            tc::mbar_arrive(&bars->sh_ready[(j + 1) & 1]);
+        }
+    } else {
+        // ---- warps 12..15: Z epilogue, W' scaling, output copy
+        const int q = warp & 3, v = tid - 384;
+        auto z_epilogue = [&](int m) -> bool {
+            // the Z slot m & 1 last held Z_{m-2}, read by the chain MMA of chunk m - 2
+            bool okw = wait(&bars->z, (m - 1) & 1) && (m < 2 || wait(&bars->delta_ready[m & 1], ((m - 2) >> 1) & 1)) &&
+                       wait(&bars->w[m & 3], (m >> 2) & 1) && wait(&bars->kt[(m - 1) & 3], ((m - 1) >> 2) & 1);
+            if (!__all_sync(0xffffffffu, okw)) return false;
+            tc::tc_fence_after();
+            unsigned char* zimg = sm + SM_Z + 8192u * (m & 1);
+            const uint32_t rp = 16 * q + (lane & 15);   // the row r' of Z this lane holds (lanes 0..15)
 #pragma unroll
-                    for (int s = 0; s < C / 8; ++s)
-                        tc::mma_tf32_ts(tmem + kT_SC, tmem + kT_DD + 8 * s, tc::smem_desc(sKT + 256 * s, 128, 2048), kId128, s > 0);
-                    tc::mma_commit(&bars->mma_c);
-                }
-            }
-            // S^T <- S^T Diag(e^{G_L}) + Delta^T Ktil on this group's columns; tf32 copy -> buffer
-            // (i + 1) & 1, which (b) of chunk i - 1 reads
-            {
-                bool okc = wait(&bars->mma_c, ph);
-                if (okc && i >= 1) okc = wait(&bars->out_ready[(i - 1) & 1u], ((i - 1) >> 1) & 1u);
-                tc::tc_fence_after();
-                if (okc && tid == 0 && ch + 1 < c_end) load(&bars->kt, TcRec::KT, TcRec::KT, 32768, ch + 1);
-                if (okc) {
-                    const uint32_t sop = kT_SOP + 128 * (b ^ 1u) + DH * g;
-#pragma unroll
-                    for (int c = 0; c < DH; c += 16) {
-                        float d[16];
-                        tc::tmem_ld16(tmem + lane + kT_SC + DH * g + c, d);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            S[c + j] = fmaf(S[c + j], s_gl[DH * g + c + j], d[j]);
-                            d[j] = tc::round_tf32(S[c + j]);
-                        }
-                        tc::tmem_st16_nowait(tmem + lane + sop + c, d);
-                    }
-                    tc::tmem_wait_st();
-                    if (a.snap) {                        // state after this chunk
-                        if (ch < a.snap_cap) {
-                            float* Sd = a.snap + (((size_t)ch * H + h) * D + v) * (size_t)D + DH * g;
-#pragma unroll
-                            for (int c = 0; c < DH; c += 4)
-                                *reinterpret_cast<float4*>(Sd + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
-                        } else if (tid == 0) {
-                            record_error(kDevErrSeqlens);
-                        }
-                    }
+            for (int c0 = 0; c0 < C; c0 += 16) {
+                float d[16];
+                tc::tmem_ld16(tmem + lane_base + T_DZ + c0, d);
+                if (lane < 16) {
+                    *reinterpret_cast<uint4*>(zimg + h64(rp, c0)) = tc::pack8_f16(d);
+                    *reinterpret_cast<uint4*>(zimg + h64(rp, c0 + 8)) = tc::pack8_f16(d + 8);
                 }
             }
             tc::tc_fence_before();
-            if (chain_sync_any(*s_abort != 0)) break;
-        }
-        const bool aborted = chain_sync_any(*s_abort != 0);
-        if (aborted) {
-            // A wait gave up: record it, let this side's MMAs and copies land.  The slot is left as it was.
-            if (tid == 0) {
-                record_error(kDevErrTimeout);
-                drain(&bars->drain[0]);
-            }
-        } else {
-            float* Sd = a.pool + ((size_t)slot * H + h) * (size_t)D * D + (size_t)v * D + DH * g;
+            tc::mbar_arrive(&bars->dz_free);
+            // W'_m = W_m Diag(gamma_{m-1}), in place: 16-byte chunk f holds W[r0 .. r0 + 7][c]
+            const float* gl = reinterpret_cast<const float*>(sm + SM_GL + 512u * ((m - 1) & 3));
+            unsigned char* wimg = sm + SM_W + 16384u * (m & 3);
+#pragma unroll 2
+            for (int f = v; f < 1024; f += 128) {
+                const float gm = gl[((f >> 6) << 3) + (f & 7)];
+                uint4 x = *reinterpret_cast<const uint4*>(wimg + 16 * f);
+                uint32_t* xs = reinterpret_cast<uint32_t*>(&x);
 #pragma unroll
-            for (int c = 0; c < DH; c += 4) *reinterpret_cast<float4*>(Sd + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+                for (int t = 0; t < 4; ++t) {
+                    float lo, hi;
+                    tc::unpack_f16x2(xs[t], lo, hi);
+                    xs[t] = tc::pack_f16x2(lo * gm, hi * gm);
+                }
+                *reinterpret_cast<uint4*>(wimg + 16 * f) = x;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc::mbar_arrive(&bars->zw_ready[(m - 1) & 1]);
+            return true;
+        };
+        auto out_copy = [&](int i) -> bool {
+            bool okw = wait(&bars->o[i & 1], (i >> 1) & 1);
+            if (!__all_sync(0xffffffffu, okw)) return false;
+            tc::tc_fence_after();
+            const int64_t t0 = a.chunk_start[c_begin + i];
+            const int L = a.chunk_len[c_begin + i];
+#pragma unroll
+            for (int r0 = 0; r0 < C; r0 += 16) {
+                float o[16];
+                tc::tmem_ld16(tmem + lane_base + T_DO + r0, o);
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                    if (r0 + t < L) out[((size_t)(t0 + r0 + t) * H + h) * D + v] = from_f32<TOut>(o[t]);
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(&bars->do_free);
+            return true;
+        };
+        bool ok = n < 2 || z_epilogue(1);
+        for (int i = 0; ok && i < n; ++i) {
+            if (i + 2 < n && !(ok = z_epilogue(i + 2))) break;
+            ok = out_copy(i);
         }
-        __syncwarp();
     }
+
     tc::tc_fence_before();
     __syncthreads();
+    const bool aborted = *s_abort != 0;
+    if (aborted) {
+        if (tid == 0) record_error(kDevErrTimeout);   // the slot is left as it was
+    } else if (warp >= 4 && warp < 12) {
+        const int g = (warp - 4) >> 2, v = tid & (D - 1);
+        float* Sd = a.pool + ((size_t)slot * H + h) * (size_t)D * D + (size_t)v * D + 64 * g;
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) *reinterpret_cast<float4*>(Sd + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+    }
     if (warp == 0) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, 512);
@@ -1120,6 +1143,11 @@ __device__ __forceinline__ void ld2x2(const float* p, uint64_t& lo, uint64_t& hi
     lo = v.x;
     hi = v.y;
 }
+// byte offset of element (row, k) of a 64-wide fp16 record image: [row/8][k/8][row%8][k%8]
+__device__ __forceinline__ uint32_t rec_h64(uint32_t row, uint32_t k)
+{
+    return (row >> 3) * 1024u + (k >> 3) * 128u + (row & 7u) * 16u + (k & 7u) * 2u;
+}
 // Gram row m (0..95) -> row block I and key row j
 __device__ __forceinline__ void gram_row(int m, int& I, int& j)
 {
@@ -1132,7 +1160,7 @@ __device__ __forceinline__ void gram_row(int m, int& I, int& j)
 // One CTA of 256 threads per (chunk, head) with 105 KB of shared memory and 256 TMEM columns, so
 // that two CTAs share an SM and each one's loads, barriers and single-thread MMA issue overlap the
 // other's arithmetic.  Three [C][LD] fp32 tiles hold k_hat, q_hat and alpha; each is reused in
-// place as the pass over it ends.  It writes the tensor-core record (TcRec) that the state pass reads:
+// place as the pass over it ends.  It writes the tensor-core record (HRec) that the state pass reads:
 //   1. loads; alpha = e^{g} (MUFU form of the gate); L2 norms fused into the loads
 //   2. diagonal 16 x 16 sub-blocks of A and P by running products of alphas (CUDA cores); each
 //      thread takes key rows j and 15 - j so that all warps do the same number of rows; P goes
@@ -1219,7 +1247,7 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
 
     // record fields, addressed from one base pointer where they are written
     unsigned char* const rec = reinterpret_cast<unsigned char*>(a.ws + ((size_t)ch * H + h) * a.ws_stride);
-#define KDA_REC(field) reinterpret_cast<float*>(rec + TcRec::field)
+#define KDA_REC(field) (rec + HRec::field)
 
     if (warp == 0) {
         tc::tmem_alloc(s_tmem, 256);
@@ -1368,19 +1396,28 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
                 }
             }
             // lane cg holds the totals of sums 4 cg .. 4 cg + 3 (0..15: A rows, 16..31: P rows)
+            if (cg < 4) {
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const int idx = 4 * cg + t, rr = idx & 15, r = blk0 + rr;
-                if (idx < 16) sAD[r * 16 + (j & 15)] = r > j ? sBeta[r] * red[t] : 0.f;
-                else KDA_REC(P)[tc::img_index(r, j, C)] = r >= j ? tc::round_tf32(red[t]) : 0.f;
+                for (int t = 0; t < 4; ++t) {
+                    const int r = blk0 + 4 * cg + t;
+                    sAD[r * 16 + (j & 15)] = r > j ? sBeta[r] * red[t] : 0.f;
+                }
+            } else {           // P rows r0 .. r0 + 3 of key column j: 8 contiguous bytes of the image
+                const int r0 = blk0 + 4 * (cg - 4);
+                float pv[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) pv[t] = r0 + t >= j ? red[t] : 0.f;
+                *reinterpret_cast<uint2*>(KDA_REC(P) + rec_h64(j, r0)) =
+                    make_uint2(tc::pack_f16x2(pv[0], pv[1]), tc::pack_f16x2(pv[2], pv[3]));
             }
         }
-        // zero upper off-diagonal blocks of the P image: (I, J) = (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
-        for (int e = tid; e < 6 * 64; e += THREADS) {
-            const int b = e >> 6, i = (e >> 2) & 15, q4 = e & 3;
+        // zero the upper off-diagonal blocks of the P image: (I, J) = (0,1) (0,2) (0,3) (1,2) (1,3) (2,3);
+        // per key column j of block J, rows 16 I .. 16 I + 15 are two 16-byte pieces
+        for (int e = tid; e < 6 * 32; e += THREADS) {
+            const int b = e >> 5, jj = (e >> 1) & 15, hf = e & 1;
             const int I = b < 3 ? 0 : (b < 5 ? 1 : 2);
             const int J = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
-            st4(KDA_REC(P) + tc::img_index(16 * I + i, 16 * J + 4 * q4, C), make_float4(0.f, 0.f, 0.f, 0.f));
+            *reinterpret_cast<uint4*>(KDA_REC(P) + rec_h64(16 * J + jj, 16 * I + 8 * hf)) = make_uint4(0, 0, 0, 0);
         }
     }
     __syncthreads();
@@ -1400,7 +1437,7 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
         sBp[(2 * hf) * D + c] = hf ? bp[2] : bp[0];
         sBp[(2 * hf + 1) * D + c] = hf ? bp[3] : bp[1];
         if (hf == 0) {
-            KDA_REC(GL)[c] = ((bp[0] * bp[1]) * bp[2]) * bp[3];
+            reinterpret_cast<float*>(KDA_REC(GL))[c] = ((bp[0] * bp[1]) * bp[2]) * bp[3];
             sB12[c] = bp[1] * bp[2];
         }
 #pragma unroll
@@ -1427,13 +1464,12 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
             for (int rr = 15; rr >= 0; --rr) {
                 const float ko = kk[rr] * rout;
                 sAl[(16 * blk + rr) * LD + c] = ko;
-                kt[rr] = tc::round_tf32(ko * ea);
+                kt[rr] = ko * ea;
                 rout *= al[rr];
             }
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-                st4(KDA_REC(KT) + tc::img_index(c, 16 * blk + 4 * q4, C),
-                    make_float4(kt[4 * q4], kt[4 * q4 + 1], kt[4 * q4 + 2], kt[4 * q4 + 3]));
+            // Ktil^T image row c, K = r: rows 16 blk .. 16 blk + 15 are two 16-byte pieces
+            *reinterpret_cast<uint4*>(KDA_REC(KT) + rec_h64(c, 16 * blk)) = tc::pack8_f16(kt);
+            *reinterpret_cast<uint4*>(KDA_REC(KT) + rec_h64(c, 16 * blk + 8)) = tc::pack8_f16(kt + 8);
             float kb[16];
             float rin = 1.f;
 #pragma unroll
@@ -1478,9 +1514,12 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
         bimg[i][2] = tc::pack_f16x2(x1.x, x1.y);
         bimg[i][3] = tc::pack_f16x2(x1.z, x1.w);
     }
-    for (int f = tid; f < C * D / 4; f += THREADS) {          // Qbar: rows r, K = c
-        const int core = f >> 3, rr = (core >> 5) * 8 + (f & 7), c = (core & 31) * 4;
-        st4(KDA_REC(QB) + 4 * f, rnd4(mul4(ld4(sQ + rr * LD + c), ld4(sEb + (rr >> 4) * D + c))));
+    for (int f = tid; f < C * D / 8; f += THREADS) {          // Qbar: rows r, K = c; 16-byte piece f
+        const int core = f >> 3, rr = (core >> 4) * 8 + (f & 7), c = (core & 15) * 8;
+        const float4 a0 = mul4(ld4(sQ + rr * LD + c), ld4(sEb + (rr >> 4) * D + c));
+        const float4 a1 = mul4(ld4(sQ + rr * LD + c + 4), ld4(sEb + (rr >> 4) * D + c + 4));
+        const float x8[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        *reinterpret_cast<uint4*>(KDA_REC(QB) + 16 * f) = tc::pack8_f16(x8);
     }
     if ((warp & 3) < 3) {          // lanes 0..95: key j decayed to the start of row block I, fp16 pairs
         const int m = (warp & 3) * 32 + lane;
@@ -1561,12 +1600,15 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
         float ga[16], gb[16];
         tc::tmem_ld16(tmem + lane_base + T_G + 32 * (Ia - 1) + 16 * hf, ga);
         tc::tmem_ld16(tmem + lane_base + T_G + 32 * (Ib - 1) + 16 * hf, gb);
+        float g[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int r = 16 * I + i;
-            const float g = I == Ia ? ga[i] : gb[i];
-            if (hf == 0) sA[r * LDA + j] = sBeta[r] * g;
-            else KDA_REC(P)[tc::img_index(r, j, C)] = tc::round_tf32(g);
+        for (int i = 0; i < 16; ++i) g[i] = I == Ia ? ga[i] : gb[i];
+        if (hf == 0) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sA[(16 * I + i) * LDA + j] = sBeta[16 * I + i] * g[i];
+        } else {      // P rows 16 I .. 16 I + 15 of key column j: two 16-byte pieces of the image
+            *reinterpret_cast<uint4*>(KDA_REC(P) + rec_h64(j, 16 * I)) = tc::pack8_f16(g);
+            *reinterpret_cast<uint4*>(KDA_REC(P) + rec_h64(j, 16 * I + 8)) = tc::pack8_f16(g + 8);
         }
     }
     tc::tmem_wait_st();
@@ -1663,12 +1705,12 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
             for (int r0 = 0; r0 < C; r0 += 16) {
                 float x[16];
                 tc::tmem_ld16(taddr + r0, x);
-                if (hf == 0) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) KDA_REC(U)[(r0 + j) * D + row] = x[j];
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) KDA_REC(W)[tc::img_index(r0 + j, row, D)] = tc::round_tf32(x[j]);
+                if (hf == 0) {        // U [r/8][v][r%8]: rows r0 .. r0 + 15 of value column v = row
+                    *reinterpret_cast<uint4*>(KDA_REC(U) + (((r0 >> 3) * D + row) << 4)) = tc::pack8_f16(x);
+                    *reinterpret_cast<uint4*>(KDA_REC(U) + ((((r0 >> 3) + 1) * D + row) << 4)) = tc::pack8_f16(x + 8);
+                } else {              // W (MN-major): rows r0 .. r0 + 15 of key column c = row
+                    *reinterpret_cast<uint4*>(KDA_REC(W) + rec_h64(row, r0)) = tc::pack8_f16(x);
+                    *reinterpret_cast<uint4*>(KDA_REC(W) + rec_h64(row, r0 + 8)) = tc::pack8_f16(x + 8);
                 }
             }
         }
@@ -1695,7 +1737,11 @@ cudaError_t run_prefill(const kda_params& p, const GateParams& gp, const void* q
                         cudaStream_t stream, const cudaEvent_t* ev, float* snap, int64_t snap_cap)
 {
     const int H = p.num_heads;
-    const WsLayout w = ws_layout(C, D, H, N, T);
+    // bf16 inputs at the 64 x 128 shape take the tensor-core pair; fp32 inputs keep the fp32 pair:
+    // 11-bit operands (unit roundoff 2^-12) cannot meet the 1e-5 relative bound that fp32 I/O
+    // carries, while they sit well inside the 2e-3 bound of bf16 I/O.
+    constexpr bool kTensorCore = (C == HRec::C && D == HRec::D && std::is_same<TIn, __nv_bfloat16>::value);
+    const WsLayout w = ws_layout(C, D, H, N, T, kTensorCore);
     int32_t* tab = reinterpret_cast<int32_t*>(workspace);
     int32_t* chunk_seq = tab;
     int32_t* chunk_start = tab + w.max_chunks;
@@ -1717,10 +1763,6 @@ cudaError_t run_prefill(const kda_params& p, const GateParams& gp, const void* q
     ia.chunk_seq = chunk_seq; ia.chunk_start = chunk_start; ia.chunk_len = chunk_len; ia.seq_off = seq_off;
     ia.state_idx = state_idx; ia.num_slots = num_slots; ia.max_chunks = w.max_chunks; ia.N = N; ia.H = H;
     ia.gp = gp; ia.ws = ws; ia.ws_stride = w.per_chunk_head;
-    // bf16 inputs at the 64 x 128 shape take the tensor-core (tf32) state pass.  fp32 inputs keep
-    // the fp32 SIMT pass: tf32 operands (unit roundoff 2^-11) cannot meet the 1e-5 relative bound
-    // that fp32 I/O carries, while they sit well inside the 2e-3 bound of bf16 I/O.
-    constexpr bool kTensorCore = (C == TcRec::C && D == TcRec::D && std::is_same<TIn, __nv_bfloat16>::value);
     dim3 gi((unsigned)w.max_chunks, (unsigned)H);
     if constexpr (kTensorCore) {
         e = cudaFuncSetAttribute(chunk_intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)itc::BYTES);
@@ -1731,7 +1773,7 @@ cudaError_t run_prefill(const kda_params& p, const GateParams& gp, const void* q
         chunk_intra_tc_kernel<<<gi, itc::THREADS, itc::BYTES, stream>>>(ia);
     } else {
         using IS = IntraShape<C, D>;
-        auto intra = chunk_intra_kernel<C, D, TIn, false>;
+        auto intra = chunk_intra_kernel<C, D, TIn>;
         e = cudaFuncSetAttribute(intra, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)IS::BYTES);
         if (e != cudaSuccess) return e;
         intra<<<gi, IS::THREADS, IS::BYTES, stream>>>(ia);
@@ -1748,9 +1790,9 @@ cudaError_t run_prefill(const kda_params& p, const GateParams& gp, const void* q
     sa.snap = snap; sa.snap_cap = snap_cap;
     if constexpr (kTensorCore) {
         auto state = chunk_state_tc_kernel<TOut>;
-        e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmemBytes);
+        e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stc::BYTES);
         if (e != cudaSuccess) return e;
-        state<<<(unsigned)((int64_t)N * H), kStateThreads, kTcSmemBytes, stream>>>(sa);
+        state<<<(unsigned)((int64_t)N * H), stc::THREADS, stc::BYTES, stream>>>(sa);
     } else {
         constexpr int NV = D < 32 ? D : 32;
         using SS = StateShape<C, D, NV>;
@@ -1796,7 +1838,8 @@ bool prefill_supported(const kda_params& p)
 
 size_t prefill_workspace_bytes(const kda_params& p, int32_t num_seqs, int64_t total_tokens)
 {
-    return ws_layout(p.chunk_size, p.head_dim, p.num_heads, num_seqs, total_tokens).total_bytes;
+    const bool tc = p.chunk_size == HRec::C && p.head_dim == HRec::D && p.io_dtype == KDA_BF16;
+    return ws_layout(p.chunk_size, p.head_dim, p.num_heads, num_seqs, total_tokens, tc).total_bytes;
 }
 
 cudaError_t launch_prefill(const kda_params& p, const GateParams& gp, const void* q,

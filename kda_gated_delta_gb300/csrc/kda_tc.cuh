@@ -38,7 +38,10 @@ __device__ __forceinline__ float round_tf32(float x)
 }
 
 // ---- descriptors ------------------------------------------------------------------------------
-// Shared-memory matrix descriptor (no swizzle, K-major, descriptor version 1).
+// Shared-memory matrix descriptor (no swizzle, descriptor version 1).  In both major-nesses the
+// leading byte offset (LBO) is the distance between core matrices adjacent along K and the stride
+// byte offset (SBO) the distance between core matrices adjacent along M (or N).  A K-major core
+// matrix is 8 rows of M/N x 16 bytes of K; an MN-major one is 8 rows of K x 16 bytes of M/N.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes)
 {
     uint64_t d = 0;
@@ -60,12 +63,16 @@ __host__ __device__ constexpr uint32_t idesc_tf32(uint32_t M, uint32_t N)
          | ((M >> 4) << 24);    // M / 16
 }
 
-// Instruction descriptor of kind::f16 with fp16 A and B (both K-major) and an fp32 accumulator.
-__host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N)
+// Instruction descriptor of kind::f16 with fp16 A and B and an fp32 accumulator.  a_mn / b_mn select
+// the MN-major ("transposed") shared-memory layout for A / B; K-major otherwise.  An A operand in
+// TMEM is always K-major.
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N, bool a_mn = false, bool b_mn = false)
 {
-    return (1u << 4)            // D format: f32
-         | ((N >> 3) << 17)     // N / 8   (A and B format 0 = f16)
-         | ((M >> 4) << 24);    // M / 16
+    return (1u << 4)                  // D format: f32
+         | (a_mn ? (1u << 15) : 0u)   // A major-ness
+         | (b_mn ? (1u << 16) : 0u)   // B major-ness
+         | ((N >> 3) << 17)           // N / 8   (A and B format 0 = f16)
+         | ((M >> 4) << 24);          // M / 16
 }
 
 // Two fp32 values rounded to fp16 (nearest even) and packed: lo in bits 0..15, hi in 16..31.
@@ -177,6 +184,18 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
         : "memory");
 }
 
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T    (kind::f16, both operands in shared memory)
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive (once) on *bar when every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar)
 {
@@ -231,7 +250,28 @@ __device__ __forceinline__ void tmem_st16u_nowait(uint32_t taddr, const uint32_t
         "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
 }
+__device__ __forceinline__ void tmem_st8u_nowait(uint32_t taddr, const uint32_t* v)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+        : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Eight fp32 values rounded to fp16 (nearest even) as one 16-byte vector, element i at bytes 2i.
+__device__ __forceinline__ uint4 pack8_f16(const float* x)
+{
+    return make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
+                      pack_f16x2(x[6], x[7]));
+}
+// The two fp16 halves of a packed pair as fp32 (lo = bits 0..15).
+__device__ __forceinline__ void unpack_f16x2(uint32_t p, float& lo, float& hi)
+{
+    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(p));
+}
 
 }  // namespace tc
 }  // namespace kda

@@ -96,10 +96,18 @@ def test_verify_validation(L):
 def test_prefill_validation_and_workspace(L):
     p = _params(D=128, chunk_size=64)
     ws = binding.prefill_workspace_size(p, 8, 16384)
-    # one record per (chunk, head) bound: ceil(T/C) + N chunks
-    per = 4 * 64 * 128 + 64 * 64 + 128
-    per = (per + 63) // 64 * 64
-    assert ws >= 4 * per * (16384 // 64 + 8) * 4
+    # one record per (chunk, head), bound ceil(T/C) + N chunks.  bf16 inputs at C = 64, D = 128: the
+    # tensor-core pair's fp16 record, five operand images (W, Ktil^T, Qbar, U: 64 x 128; P: 64 x 64)
+    # and e^{G_L} in fp32; other shapes: the fp32 record W, Qbar, Ktil, U, P and e^{G_L}.
+    nrec = 4 * (16384 // 64 + 8)
+    per_tc = 2 * (4 * 64 * 128 + 64 * 64) + 4 * 128
+    per_f32 = 4 * ((4 * 64 * 128 + 64 * 64 + 128 + 63) // 64 * 64)
+    p.io_dtype = binding.KDA_BF16
+    assert binding.prefill_workspace_size(p, 8, 16384) >= per_tc * nrec
+    assert binding.prefill_workspace_size(p, 8, 16384) < per_tc * nrec + 64 * 1024
+    p.io_dtype = binding.KDA_F32
+    assert binding.prefill_workspace_size(p, 8, 16384) >= per_f32 * nrec
+    assert ws > 0
     assert binding.prefill_workspace_size(_params(D=48), 8, 100) == 0
     f = L.kda_chunk_prefill
 
