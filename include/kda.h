@@ -258,8 +258,8 @@ int32_t kda_commit_verified_states(const kda_params* p,
  * loading from the first call of this entry point on that device, under eager loading
  * (CUDA_MODULE_LOADING=EAGER) from the creation of the context.  The call allocates nothing.  A problem whose kda_chunk_prefill_workspace_size(...) exceeds
  * KDA_STATIC_SCRATCH_BYTES is rejected with KDA_ERR_SCRATCH_LIMIT before any work is enqueued
- * (with H = 32, head_dim = 128, chunk 64 the array covers ceil(T / 64) + num_seqs <= 56 chunks,
- * about 3,000 tokens per call).
+ * (with bf16 inputs, H = 32, head_dim = 128, chunk 64 the array covers ceil(T / 64) + num_seqs
+ * <= 112 chunks, about 7,000 tokens per call).
  *
  * Every call looks up the device address of the array in the current context (nothing is
  * cached, so a context that was reset and created again is handled); under lazy loading the

@@ -663,10 +663,14 @@ __global__ void __launch_bounds__(256, 1) chunk_state_kernel(const StateArgs a)
 //   warps 0..3    Delta pass: Delta_i^T = U_i^T - (chain accumulator), rounded to fp16, into TMEM
 //   warps 4..11   S update (fp32 in registers, two groups of 64 key columns) and its fp16 copy
 //   warps 12..15  Z epilogue (Z_j accumulator -> fp16 operand image), W'_j scaling, output copy
-//   warp 16       issues the chain MMA and (c) = Delta^T Ktil, and the record copies W, Ktil, U
-//   warp 17       issues Z_j and the output MMAs, and the Qbar / P copies
+//   warp 16       issues the chain MMA, then (c) = Delta^T Ktil (the tensor core runs one thread's MMAs
+//                 in issue order, so the chain MMA is never delayed by (c))
+//   warp 17       issues Z_j and the output MMAs
+//   warp 18       issues the record copies (W, Ktil^T + gamma, U, Qbar + P), each as soon as its slot
+//                 is free; the MMA issuers never issue copies
 // Operands in TMEM (fp16 pairs): S^T (two buffers), Delta^T (two buffers); accumulators (fp32): the
-// chain, (c), the output and Z.  Operand images arrive by bulk copy straight from the record.
+// chain, (c), the output and Z.  Operand images arrive by bulk copy straight from the record; the
+// MMA issuers never issue copies, so a slow copy issue never delays an MMA.
 // Hand-offs are mbarriers: MMA completions by tcgen05.commit, the passes by thread arrivals.  Every
 // wait is bounded and gives up early once any thread has recorded a failure; a role that gives up
 // leaves its loop, the issuers let their MMAs and copies land (bounded), and the slot is left as it
@@ -680,12 +684,14 @@ constexpr uint32_t SM_U = 131072;       // 2 x 16384: U_j; slot j % 2
 constexpr uint32_t SM_QB = 163840;      // 16384: Qbar_j, followed by P_j (one copy)
 constexpr uint32_t SM_P = 180224;       // 8192
 constexpr uint32_t SM_Z = 188416;       // 2 x 8192: Z_j image; slot j % 2
-constexpr uint32_t SM_GL = 212992;      // 4 x 512: gamma_j, copied with Ktil^T_j; slot j % 4
-constexpr uint32_t SM_BAR = 215040;     // mbarriers
+constexpr uint32_t SM_GL = 204800;      // 4 x 512: gamma_j, copied with Ktil^T_j; slot j % 4
+constexpr uint32_t SM_BAR = 206848;     // mbarriers
 constexpr uint32_t SM_MISC = SM_BAR + 256;
-constexpr uint32_t BYTES = SM_MISC + 64;
-constexpr int THREADS = 576;
-static_assert(SM_QB + 16384 == SM_P && SM_P + 8192 == SM_Z, "layout");
+constexpr uint32_t SM_OUT = 208896;     // 16384: output rows staged for the bulk stores
+constexpr uint32_t BYTES = SM_OUT + 16384;
+constexpr int THREADS = 608;
+static_assert(SM_QB + 16384 == SM_P && SM_P + 8192 == SM_Z && SM_Z + 16384 == SM_GL, "layout");
+static_assert(SM_MISC + 64 <= SM_OUT, "layout");
 static_assert(BYTES <= 232448, "state-pass shared memory");
 // TMEM columns (512 allocated; each accumulator starts at a multiple of its width)
 constexpr uint32_t T_SH = 0;     // fp16 S^T, two buffers (2 x 64 cols)
@@ -703,8 +709,8 @@ struct StBars {
     uint64_t z;                       // Z_j complete                         (warp 17 commit)
     uint64_t o[2];                    // outputs of chunk i complete, i & 1   (warp 17 commit)
     uint64_t delta_ready[2];          // Delta_j in TMEM, index j & 1         (128 arrivals)
-    uint64_t sh_ready[2];             // S_j done (fp16 copy in TMEM), j & 1  (256 arrivals)
-    uint64_t zw_ready[2];             // Z_j image and W'_j ready, (j-1) & 1  (128 arrivals)
+    uint64_t sh_ready[4];             // S_j done (fp16 copy in TMEM), j & 3  (256 arrivals)
+    uint64_t zw_ready[4];             // Z_j image and W'_j ready, (j-1) & 3  (128 arrivals)
     uint64_t dz_free;                 // Z accumulator read                   (128 arrivals)
     uint64_t do_free;                 // output accumulator read              (128 arrivals)
     uint64_t drain[2];                // each issuer's final completion wait
@@ -764,10 +770,8 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
         tc::mbar_init(&bars->u[0], 1); tc::mbar_init(&bars->u[1], 1); tc::mbar_init(&bars->qp, 1);
         tc::mbar_init(&bars->chain, 1); tc::mbar_init(&bars->c, 1); tc::mbar_init(&bars->z, 1);
         tc::mbar_init(&bars->o[0], 1); tc::mbar_init(&bars->o[1], 1);
-        for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(&bars->delta_ready[i], 128); tc::mbar_init(&bars->sh_ready[i], 256);
-            tc::mbar_init(&bars->zw_ready[i], 128);
-        }
+        tc::mbar_init(&bars->delta_ready[0], 128); tc::mbar_init(&bars->delta_ready[1], 128);
+        for (int i = 0; i < 4; ++i) { tc::mbar_init(&bars->sh_ready[i], 256); tc::mbar_init(&bars->zw_ready[i], 128); }
         tc::mbar_init(&bars->dz_free, 128); tc::mbar_init(&bars->do_free, 128);
         tc::mbar_init(&bars->drain[0], 1); tc::mbar_init(&bars->drain[1], 1);
         *s_abort = 0;
@@ -795,79 +799,56 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
     float S[D / 2];   // the S update threads: columns 64 g .. 64 g + 63 of row v of S^T (fp32)
 
     if (warp >= 16) {
-        // ---- the two issuers (lane 0 of warps 16 and 17); copies in flight are tracked per barrier
+        // ---- the two MMA issuers and the loader (lane 0 of warps 16, 17, 18)
         if (lane == 0) {
-            uint64_t* const lbar0 = &bars->w[0];          // w[4], kt[4], u[2], qp: 11 load barriers
-            uint32_t uses[11] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
-            auto issue = [&](uint64_t* bar, int j, uint32_t dst, uint32_t src, uint32_t bytes, uint32_t dst2,
-                             uint32_t src2, uint32_t bytes2) {
-                ++uses[bar - lbar0];
-                tc::mbar_arrive_expect_tx(bar, bytes + bytes2);
-                tc::bulk_g2s(sm + dst, rec_of(j) + src, bytes, bar);
-                if (bytes2) tc::bulk_g2s(sm + dst2, rec_of(j) + src2, bytes2, bar);
-            };
             bool ok = true;
             const int me = warp - 16;
             if (me == 0) {
-                // ---- warp 16: chain MMA and (c); copies of W, Ktil^T + gamma, U
-                auto load_w = [&](int j) { issue(&bars->w[j & 3], j, SM_W + 16384u * (j & 3), HRec::W, 16384, 0, 0, 0); };
-                auto load_kt = [&](int j) {
-                    issue(&bars->kt[j & 3], j, SM_KT + 16384u * (j & 3), HRec::KT, 16384, SM_GL + 512u * (j & 3), HRec::GL, 512);
-                };
-                auto load_u = [&](int j) { issue(&bars->u[j & 1], j, SM_U + 16384u * (j & 1), HRec::U, 16384, 0, 0, 0); };
+                // ---- warp 16: the chain MMA, then (c)
                 constexpr uint32_t idChainS = tc::idesc_f16(128, 64, false, true);   // B = W' (MN-major)
                 constexpr uint32_t idChainZ = tc::idesc_f16(128, 64);                // B = Z (K-major)
                 constexpr uint32_t idC = tc::idesc_f16(128, 128);                    // B = Ktil^T (K-major)
-                for (int j = 0; j < 4 && j < n; ++j) load_w(j);
-                for (int j = 0; j < 3 && j < n; ++j) load_kt(j);
-                for (int j = 0; j < 2 && j < n; ++j) load_u(j);
                 // chain MMA of chunk 0: S_0 W_0^T
                 ok = wait(&bars->sh_ready[0], 0) && wait(&bars->w[0], 0);
                 if (ok) {
                     tc::tc_fence_after();
+                    const uint64_t dw = desc(sm + SM_W, 1024, 128);
 #pragma unroll
                     for (int s = 0; s < D / 16; ++s)
-                        tc::mma_f16_ts(tmem + T_DA, tmem + T_SH + 8 * s, desc(sm + SM_W + 2048 * s, 1024, 128), idChainS, s > 0);
+                        tc::mma_f16_ts(tmem + T_DA, tmem + T_SH + 8 * s, dw + (uint64_t)(128 * s), idChainS, s > 0);
                     tc::mma_commit(&bars->chain);
                 }
                 for (int i = 0; ok && i < n; ++i) {
-                    // Delta_i is in TMEM; S_i is done (so the update pass is done reading (c) of i - 1)
-                    if (!(ok = wait(&bars->delta_ready[i & 1], (i >> 1) & 1) && wait(&bars->sh_ready[i & 1], (i >> 1) & 1)))
+                    // Delta_i is in TMEM (the Delta pass has read the chain accumulator); S_i is done (the
+                    // update pass has read (c) of i - 1)
+                    if (!(ok = wait(&bars->delta_ready[i & 1], (i >> 1) & 1) && wait(&bars->sh_ready[i & 3], (i >> 2) & 1)))
                         break;
+                    const uint32_t dh = tmem + T_DH + 32 * (i & 1);
                     if (i + 1 < n) {   // chain MMA of chunk i + 1: S_i W'^T_{i+1} + Delta_i Z^T_{i+1}
-                        if (!(ok = wait(&bars->zw_ready[i & 1], (i >> 1) & 1))) break;
+                        if (!(ok = wait(&bars->zw_ready[i & 3], (i >> 2) & 1))) break;
                         tc::tc_fence_after();
-                        const uint32_t sh = tmem + T_SH + 64 * (i & 1), dh = tmem + T_DH + 32 * (i & 1);
-                        const unsigned char* wb = sm + SM_W + 16384u * ((i + 1) & 3);
-                        const unsigned char* zb = sm + SM_Z + 8192u * ((i + 1) & 1);
+                        const uint32_t sh = tmem + T_SH + 64 * (i & 1);
+                        const uint64_t dw = desc(sm + SM_W + 16384u * ((i + 1) & 3), 1024, 128);
+                        const uint64_t dz = desc(sm + SM_Z + 8192u * ((i + 1) & 1), 128, 1024);
 #pragma unroll
-                        for (int s = 0; s < D / 16; ++s)
-                            tc::mma_f16_ts(tmem + T_DA, sh + 8 * s, desc(wb + 2048 * s, 1024, 128), idChainS, s > 0);
+                        for (int s = 0; s < D / 16; ++s)      // descriptor start advances in 16-byte units
+                            tc::mma_f16_ts(tmem + T_DA, sh + 8 * s, dw + (uint64_t)(128 * s), idChainS, s > 0);
 #pragma unroll
                         for (int s = 0; s < C / 16; ++s)
-                            tc::mma_f16_ts(tmem + T_DA, dh + 8 * s, desc(zb + 256 * s, 128, 1024), idChainZ, 1);
+                            tc::mma_f16_ts(tmem + T_DA, dh + 8 * s, dz + (uint64_t)(16 * s), idChainZ, 1);
                         tc::mma_commit(&bars->chain);
                     }
                     // (c): Delta_i^T Ktil_i
                     if (!(ok = wait(&bars->kt[i & 3], (i >> 2) & 1))) break;
                     tc::tc_fence_after();
-                    {
-                        const uint32_t dh = tmem + T_DH + 32 * (i & 1);
-                        const unsigned char* kb = sm + SM_KT + 16384u * (i & 3);
+                    const uint64_t dk = desc(sm + SM_KT + 16384u * (i & 3), 128, 1024);
 #pragma unroll
-                        for (int s = 0; s < C / 16; ++s)
-                            tc::mma_f16_ts(tmem + T_DC, dh + 8 * s, desc(kb + 256 * s, 128, 1024), idC, s > 0);
-                        tc::mma_commit(&bars->c);
-                    }
-                    // slots freed this step: W_i (its chain MMA is done), U_i (read by the Delta pass),
-                    // Ktil_{i-1} and gamma_{i-1} (their last readers signalled sh_ready(i) / zw_ready(i))
-                    if (i + 4 < n) load_w(i + 4);
-                    if (i + 3 < n) load_kt(i + 3);
-                    if (i + 2 < n) load_u(i + 2);
+                    for (int s = 0; s < C / 16; ++s)
+                        tc::mma_f16_ts(tmem + T_DC, dh + 8 * s, dk + (uint64_t)(16 * s), idC, s > 0);
+                    tc::mma_commit(&bars->c);
                 }
-            } else {
-                // ---- warp 17: Z_j = W_j Ktil_{j-1}^T and the outputs; copies of Qbar + P
-                auto load_qp = [&](int j) { issue(&bars->qp, j, SM_QB, HRec::QB, 24576, 0, 0, 0); };
+            } else if (me == 1) {
+                // ---- warp 17: Z_j = W_j Ktil_{j-1}^T and the outputs
                 constexpr uint32_t idZ = tc::idesc_f16(64, 64, true, true);    // A = W, B = Ktil (both MN-major)
                 constexpr uint32_t idB2 = tc::idesc_f16(128, 64, false, true); // B = P (MN-major)
                 constexpr uint32_t idB = tc::idesc_f16(128, 64);               // B = Qbar (K-major)
@@ -876,42 +857,75 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
                           (m == 1 || wait(&bars->dz_free, (m - 2) & 1))))
                         return false;
                     tc::tc_fence_after();
-                    const unsigned char* wb = sm + SM_W + 16384u * (m & 3);
-                    const unsigned char* kb = sm + SM_KT + 16384u * ((m - 1) & 3);
+                    const uint64_t dw = desc(sm + SM_W + 16384u * (m & 3), 1024, 128);
+                    const uint64_t dk = desc(sm + SM_KT + 16384u * ((m - 1) & 3), 1024, 128);
 #pragma unroll
                     for (int s = 0; s < D / 16; ++s)
-                        tc::mma_f16_ss(tmem + T_DZ, desc(wb + 2048 * s, 1024, 128), desc(kb + 2048 * s, 1024, 128), idZ, s > 0);
+                        tc::mma_f16_ss(tmem + T_DZ, dw + (uint64_t)(128 * s), dk + (uint64_t)(128 * s), idZ, s > 0);
                     tc::mma_commit(&bars->z);
                     return true;
                 };
-                load_qp(0);
+                const uint64_t dp = desc(sm + SM_P, 1024, 128), dq = desc(sm + SM_QB, 128, 2048);
                 ok = n < 2 || issue_z(1);
                 for (int i = 0; ok && i < n; ++i) {
                     if (i + 2 < n && !(ok = issue_z(i + 2))) break;
-                    if (!(ok = wait(&bars->delta_ready[i & 1], (i >> 1) & 1) && wait(&bars->sh_ready[i & 1], (i >> 1) & 1) &&
-                               wait(&bars->qp, i & 1) &&
-                               (i == 0 || wait(&bars->do_free, (i - 1) & 1))))
+                    if (!(ok = wait(&bars->delta_ready[i & 1], (i >> 1) & 1) && wait(&bars->sh_ready[i & 3], (i >> 2) & 1) &&
+                               wait(&bars->qp, i & 1) && (i == 0 || wait(&bars->do_free, (i - 1) & 1))))
                         break;
                     tc::tc_fence_after();
                     const uint32_t sh = tmem + T_SH + 64 * (i & 1), dh = tmem + T_DH + 32 * (i & 1);
 #pragma unroll
                     for (int s = 0; s < C / 16; ++s)   // (b2) P_i Delta_i
-                        tc::mma_f16_ts(tmem + T_DO, dh + 8 * s, desc(sm + SM_P + 2048 * s, 1024, 128), idB2, s > 0);
+                        tc::mma_f16_ts(tmem + T_DO, dh + 8 * s, dp + (uint64_t)(128 * s), idB2, s > 0);
 #pragma unroll
                     for (int s = 0; s < D / 16; ++s)   // (b) + Qbar_i S_i
-                        tc::mma_f16_ts(tmem + T_DO, sh + 8 * s, desc(sm + SM_QB + 256 * s, 128, 2048), idB, 1);
+                        tc::mma_f16_ts(tmem + T_DO, sh + 8 * s, dq + (uint64_t)(16 * s), idB, 1);
                     tc::mma_commit(&bars->o[i & 1]);
-                    if (i + 1 < n) {   // Qbar and P are free once the outputs are done
+                }
+            } else {
+                // ---- warp 18: record copies, each issued once its slot's last reader is done
+                uint64_t* const lbar0 = &bars->w[0];          // w[4], kt[4], u[2], qp: 11 load barriers
+                uint32_t uses[11] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+                auto issue = [&](uint64_t* bar, int j, uint32_t dst, uint32_t src, uint32_t bytes, uint32_t dst2,
+                                 uint32_t src2, uint32_t bytes2) {
+                    ++uses[bar - lbar0];
+                    tc::mbar_arrive_expect_tx(bar, bytes + bytes2);
+                    tc::bulk_g2s(sm + dst, rec_of(j) + src, bytes, bar);
+                    if (bytes2) tc::bulk_g2s(sm + dst2, rec_of(j) + src2, bytes2, bar);
+                };
+                auto load_w = [&](int j) { issue(&bars->w[j & 3], j, SM_W + 16384u * (j & 3), HRec::W, 16384, 0, 0, 0); };
+                auto load_kt = [&](int j) {
+                    issue(&bars->kt[j & 3], j, SM_KT + 16384u * (j & 3), HRec::KT, 16384, SM_GL + 512u * (j & 3), HRec::GL, 512);
+                };
+                auto load_u = [&](int j) { issue(&bars->u[j & 1], j, SM_U + 16384u * (j & 1), HRec::U, 16384, 0, 0, 0); };
+                auto load_qp = [&](int j) { issue(&bars->qp, j, SM_QB, HRec::QB, 24576, 0, 0, 0); };
+                for (int j = 0; j < 4 && j < n; ++j) load_w(j);
+                for (int j = 0; j < 3 && j < n; ++j) load_kt(j);
+                for (int j = 0; j < 2 && j < n; ++j) load_u(j);
+                load_qp(0);
+                for (int i = 0; ok && i < n; ++i) {
+                    // Delta_i done: U_i has been read and the chain MMA of chunk i (the last reader of W_i) is done
+                    if (!(ok = wait(&bars->delta_ready[i & 1], (i >> 1) & 1))) break;
+                    if (i + 2 < n) load_u(i + 2);
+                    if (i + 4 < n) load_w(i + 4);
+                    if (i + 1 < n) {       // the outputs of chunk i are done with Qbar and P
                         if (!(ok = wait(&bars->o[i & 1], (i >> 1) & 1))) break;
                         load_qp(i + 1);
                     }
+                    if (i + 3 < n) {       // Ktil_{i-1} and gamma_{i-1}: read by (c) of i - 1, the S update
+                        if (i >= 1 &&      // of i - 1 (sh_ready(i)) and Z_i / W'_i (zw_ready(i))
+                            !(ok = wait(&bars->sh_ready[i & 3], (i >> 2) & 1) && wait(&bars->zw_ready[(i - 1) & 3], ((i - 1) >> 2) & 1)))
+                            break;
+                        load_kt(i + 3);
+                    }
                 }
+                for (int bi = 0; bi < 11; ++bi)              // copies in flight land before the CTA exits (bounded)
+                    if (uses[bi]) tc::mbar_wait(lbar0 + bi, (uses[bi] - 1) & 1u, kWaitPolls);
             }
-            // let this issuer's MMAs and copies land before the CTA exits (bounded)
-            tc::mma_commit(&bars->drain[me]);
-            tc::mbar_wait(&bars->drain[me], 0, kWaitPolls);
-            for (int bi = 0; bi < 11; ++bi)
-                if (uses[bi]) tc::mbar_wait(lbar0 + bi, (uses[bi] - 1) & 1u, kWaitPolls);
+            if (me < 2) {           // this issuer's MMAs complete before TMEM is freed (bounded)
+                tc::mma_commit(&bars->drain[me]);
+                tc::mbar_wait(&bars->drain[me], 0, kWaitPolls);
+            }
             if (!ok) *s_abort = 1;
         }
         __syncwarp();
@@ -997,7 +1011,7 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
                 }
             }
             tc::tc_fence_before();
-            tc::mbar_arrive(&bars->sh_ready[(j + 1) & 1]);
+            tc::mbar_arrive(&bars->sh_ready[(j + 1) & 3]);
         }
     } else {
         // ---- warps 12..15: Z epilogue, W' scaling, output copy
@@ -1006,7 +1020,7 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
             // the Z slot m & 1 last held Z_{m-2}, read by the chain MMA of chunk m - 2
             bool okw = wait(&bars->z, (m - 1) & 1) && (m < 2 || wait(&bars->delta_ready[m & 1], ((m - 2) >> 1) & 1)) &&
                        wait(&bars->w[m & 3], (m >> 2) & 1) && wait(&bars->kt[(m - 1) & 3], ((m - 1) >> 2) & 1);
-            if (!__all_sync(0xffffffffu, okw)) return false;
+            if (tc::bar_any<1, 128>(!okw)) return false;   // the same exit for all four warps
             tc::tc_fence_after();
             unsigned char* zimg = sm + SM_Z + 8192u * (m & 1);
             const uint32_t rp = 16 * q + (lane & 15);   // the row r' of Z this lane holds (lanes 0..15)
@@ -1038,25 +1052,45 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
                 *reinterpret_cast<uint4*>(wimg + 16 * f) = x;
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            tc::mbar_arrive(&bars->zw_ready[(m - 1) & 1]);
+            tc::mbar_arrive(&bars->zw_ready[(m - 1) & 3]);
             return true;
         };
+        // Output rows go through shared memory: each thread writes its value column of O (a TMEM
+        // lane) into the staging tile [r][v]; then the 128 threads copy the tile out in 16-byte pieces,
+        // 16 (bf16) or 32 (fp32) consecutive threads per row, rows past the chunk end skipped.  fp32
+        // rows are staged 32 at a time.
+        TOut* stage = reinterpret_cast<TOut*>(sm + SM_OUT);
+        constexpr int RH = sizeof(TOut) == 2 ? C : C / 2;
+        constexpr int PIECES_PER_ROW = D * (int)sizeof(TOut) / 16;
         auto out_copy = [&](int i) -> bool {
-            bool okw = wait(&bars->o[i & 1], (i >> 1) & 1);
-            if (!__all_sync(0xffffffffu, okw)) return false;
-            tc::tc_fence_after();
             const int64_t t0 = a.chunk_start[c_begin + i];
             const int L = a.chunk_len[c_begin + i];
+            bool okw = wait(&bars->o[i & 1], (i >> 1) & 1);
+            if (tc::bar_any<1, 128>(!okw)) return false;         // also: the tile is free again
+            tc::tc_fence_after();
 #pragma unroll
-            for (int r0 = 0; r0 < C; r0 += 16) {
-                float o[16];
-                tc::tmem_ld16(tmem + lane_base + T_DO + r0, o);
+            for (int rb = 0; rb < C; rb += RH) {
+                if (rb > 0) tc::bar_sync<1, 128>();
 #pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    if (r0 + t < L) out[((size_t)(t0 + r0 + t) * H + h) * D + v] = from_f32<TOut>(o[t]);
+                for (int r0 = rb; r0 < rb + RH; r0 += 16) {
+                    float o[16];
+                    tc::tmem_ld16(tmem + lane_base + T_DO + r0, o);
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) stage[(r0 - rb + t) * D + v] = from_f32<TOut>(o[t]);
+                }
+                if (rb + RH == C) {
+                    tc::tc_fence_before();
+                    tc::mbar_arrive(&bars->do_free);
+                }
+                tc::bar_sync<1, 128>();
+#pragma unroll
+                for (int pc = v; pc < RH * PIECES_PER_ROW; pc += 128) {
+                    const int r = rb + pc / PIECES_PER_ROW, q16 = pc % PIECES_PER_ROW;
+                    if (r < L)
+                        *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(out + ((size_t)(t0 + r) * H + h) * D) + 16 * q16) =
+                            *reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned char*>(stage) + 16 * pc);
+                }
             }
-            tc::tc_fence_before();
-            tc::mbar_arrive(&bars->do_free);
             return true;
         };
         bool ok = n < 2 || z_epilogue(1);

@@ -139,6 +139,40 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// ---- bulk async copy shared -> global (bulk-group completion) -------------------------------------
+// src and dst 16-byte aligned, bytes a multiple of 16.  The issuing thread tracks completion with
+// bulk_commit / bulk_wait_read (the shared source may be reused) / bulk_wait (writes done).
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Make this thread's generic-proxy shared-memory writes visible to the async proxy (TMA, MMA).
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Named barrier over COUNT threads that also returns, to each of them, whether any passed a true
+// flag: a loop exit decided after it is the same for every participant.
+template <int ID, int COUNT>
+__device__ __forceinline__ bool bar_any(bool flag)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)flag), "n"(ID), "n"(COUNT)
+        : "memory");
+    return r != 0;
+}
+template <int ID, int COUNT>
+__device__ __forceinline__ void bar_sync() { asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(COUNT) : "memory"); }
+
 // ---- tensor memory ------------------------------------------------------------------------------
 // Warp-wide: allocate ncols (power of two >= 32) TMEM columns; the base address goes to *dst.
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols)

@@ -85,7 +85,7 @@ def test_static_scratch_rejects_problems_beyond_its_size():
     L = _lib()
     H, D = 32, 128
     params = binding.make_params(H, D, io_dtype=torch.bfloat16, chunk_size=64)
-    T = 8192                                              # needs about 1.2 GB of scratch
+    T = 8192                                              # needs about 0.31 GB of scratch
     assert binding.prefill_workspace_size(params, 1, T) > STATIC_SCRATCH_BYTES
     q = torch.zeros(T, H, D, dtype=torch.bfloat16, device=DEV)
     g = torch.zeros(T, H, D, dtype=torch.float32, device=DEV)
