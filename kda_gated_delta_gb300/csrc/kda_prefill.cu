@@ -62,11 +62,13 @@ struct HRec {
 };
 
 // ---- workspace layout ----------------------------------------------------------------------
-// [chunk table: 3 * max_chunks + (N + 1) + N int32, padded to 256 B]
+// [chunk table: 3 * max_chunks + (N + 1) + N int32, padded to 16 B; then max_chunks int4 chunk
+//  records {sequence, first token, length, slot}; padded to 256 B]
 // [per (chunk, head) record: the fp16 HRec (tensor-core pair), or for the fp32 pair
 //  W C*D | Qbar C*D | Ktil C*D | U C*D | P C*C | gL D  floats, padded to 64]
 struct WsLayout {
     int64_t max_chunks;
+    size_t info_offset;     // bytes: the int4 chunk records
     size_t table_bytes;
     size_t per_chunk_head;  // floats
     size_t total_bytes;
@@ -79,7 +81,8 @@ WsLayout ws_layout(int C, int D, int H, int32_t N, int64_t T, bool tc)
 {
     WsLayout w;
     w.max_chunks = (T + C - 1) / C + N;
-    w.table_bytes = round_up(sizeof(int32_t) * (size_t)(3 * w.max_chunks + 2 * (int64_t)N + 1), 256);
+    w.info_offset = round_up(sizeof(int32_t) * (size_t)(3 * w.max_chunks + 2 * (int64_t)N + 1), 16);
+    w.table_bytes = round_up(w.info_offset + 16 * (size_t)w.max_chunks, 256);
     w.per_chunk_head = tc ? HRec::BYTES / sizeof(float) : round_up((size_t)4 * C * D + (size_t)C * C + D, 64);
     w.total_bytes = w.table_bytes + sizeof(float) * w.per_chunk_head * (size_t)w.max_chunks * H;
     return w;
@@ -108,9 +111,10 @@ __device__ __forceinline__ void seq_range(const int32_t* __restrict__ cu, int32_
 
 __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* __restrict__ cu, int32_t N, int64_t T,
                                                            int C, int64_t max_chunks,
+                                                           const int32_t* __restrict__ state_idx, int64_t num_slots,
                                                            int32_t* chunk_seq, int32_t* chunk_start,
                                                            int32_t* chunk_len, int32_t* seq_off,
-                                                           int32_t* seq_order)
+                                                           int32_t* seq_order, int4* chunk_info)
 {
     __shared__ int32_t s_warp[32];
     __shared__ int32_t s_base;
@@ -169,10 +173,15 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* __rest
         int64_t s0, s1;
         seq_range(cu, lo, N, T, s0, s1, false);
         const int64_t st = s0 + (c - seq_off[lo]) * C;
+        const int32_t len = (int32_t)((s1 - st) < C ? (s1 - st) : C);
         chunk_seq[c] = lo;
         chunk_start[c] = (int32_t)st;
-        chunk_len[c] = (int32_t)((s1 - st) < C ? (s1 - st) : C);
+        chunk_len[c] = len;
+        const int64_t slot = state_idx[lo];
+        chunk_info[c] = make_int4(lo, (int32_t)st, len, slot >= 0 && slot < num_slots ? (int32_t)slot : -1);
     }
+    // grid entries past the last chunk: length 0 (the intra kernel's CTAs there exit)
+    for (int64_t c = nch + tid; c < max_chunks; c += blockDim.x) chunk_info[c] = make_int4(0, 0, 0, -1);
     // 3. sequences by decreasing chunk count
     for (int32_t i = tid; i < N; i += blockDim.x) {
         if (N > kMaxSortedSeqs) {
@@ -202,6 +211,7 @@ struct IntraArgs {
     const int32_t* chunk_start;
     const int32_t* chunk_len;
     const int32_t* seq_off;   // seq_off[N] = number of chunks
+    const int4* chunk_info;   // per chunk {sequence, first token, length, slot or -1}; length 0 past the end
     const int32_t* state_idx;
     int64_t num_slots;
     int64_t max_chunks;
@@ -679,19 +689,19 @@ constexpr uint32_t kWaitPolls = 1u << 24;
 
 namespace stc {
 constexpr uint32_t SM_W = 0;            // 4 x 16384: W_j, scaled in place to W'_j; slot j % 4
-constexpr uint32_t SM_KT = 65536;       // 4 x 16384: Ktil^T_j; slot j % 4
-constexpr uint32_t SM_U = 131072;       // 2 x 16384: U_j; slot j % 2
-constexpr uint32_t SM_QB = 163840;      // 16384: Qbar_j, followed by P_j (one copy)
-constexpr uint32_t SM_P = 180224;       // 8192
-constexpr uint32_t SM_Z = 188416;       // 2 x 8192: Z_j image; slot j % 2
-constexpr uint32_t SM_GL = 204800;      // 4 x 512: gamma_j, copied with Ktil^T_j; slot j % 4
-constexpr uint32_t SM_BAR = 206848;     // mbarriers
+constexpr uint32_t SM_KT = 65536;       // 3 x 16384: Ktil^T_j; slot j % 3
+constexpr uint32_t SM_U = 114688;       // 2 x 16384: U_j; slot j % 2
+constexpr uint32_t SM_QP = 147456;      // 2 x 24576: Qbar_j (16384) followed by P_j (8192), one copy; slot j % 2
+constexpr uint32_t QP_SLOT = 24576, QP_P = 16384;
+constexpr uint32_t SM_Z = 196608;       // 2 x 8192: Z_j image; slot j % 2
+constexpr uint32_t SM_GL = 212992;      // 3 x 512: gamma_j, copied with Ktil^T_j; slot j % 3
+constexpr uint32_t SM_BAR = 214528;     // mbarriers
 constexpr uint32_t SM_MISC = SM_BAR + 256;
-constexpr uint32_t SM_OUT = 208896;     // 16384: output rows staged for the bulk stores
+constexpr uint32_t SM_OUT = SM_MISC + 64;   // 16384: output rows staged for the 16-byte stores
 constexpr uint32_t BYTES = SM_OUT + 16384;
 constexpr int THREADS = 608;
-static_assert(SM_QB + 16384 == SM_P && SM_P + 8192 == SM_Z && SM_Z + 16384 == SM_GL, "layout");
-static_assert(SM_MISC + 64 <= SM_OUT, "layout");
+static_assert(SM_KT + 3 * 16384 == SM_U && SM_U + 2 * 16384 == SM_QP && SM_QP + 2 * QP_SLOT == SM_Z &&
+              SM_Z + 2 * 8192 == SM_GL && SM_GL + 3 * 512 <= SM_BAR, "layout");
 static_assert(BYTES <= 232448, "state-pass shared memory");
 // TMEM columns (512 allocated; each accumulator starts at a multiple of its width)
 constexpr uint32_t T_SH = 0;     // fp16 S^T, two buffers (2 x 64 cols)
@@ -703,7 +713,7 @@ constexpr uint32_t T_DZ = 448;   // Z accumulator, M = 64: lane 32 (r' >> 4) + (
 }  // namespace stc
 
 struct StBars {
-    uint64_t w[4], kt[4], u[2], qp;   // record copies landed (tx bytes)
+    uint64_t w[4], kt[3], u[2], qp[2];   // record copies landed (tx bytes)
     uint64_t chain;                   // chain MMA of chunk j complete        (warp 16 commit)
     uint64_t c;                       // (c) of chunk j complete              (warp 16 commit)
     uint64_t z;                       // Z_j complete                         (warp 17 commit)
@@ -766,8 +776,9 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
         tc::tmem_relinquish();
     }
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) { tc::mbar_init(&bars->w[i], 1); tc::mbar_init(&bars->kt[i], 1); }
-        tc::mbar_init(&bars->u[0], 1); tc::mbar_init(&bars->u[1], 1); tc::mbar_init(&bars->qp, 1);
+        for (int i = 0; i < 4; ++i) tc::mbar_init(&bars->w[i], 1);
+        for (int i = 0; i < 3; ++i) tc::mbar_init(&bars->kt[i], 1);
+        for (int i = 0; i < 2; ++i) { tc::mbar_init(&bars->u[i], 1); tc::mbar_init(&bars->qp[i], 1); }
         tc::mbar_init(&bars->chain, 1); tc::mbar_init(&bars->c, 1); tc::mbar_init(&bars->z, 1);
         tc::mbar_init(&bars->o[0], 1); tc::mbar_init(&bars->o[1], 1);
         tc::mbar_init(&bars->delta_ready[0], 128); tc::mbar_init(&bars->delta_ready[1], 128);
@@ -839,9 +850,9 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
                         tc::mma_commit(&bars->chain);
                     }
                     // (c): Delta_i^T Ktil_i
-                    if (!(ok = wait(&bars->kt[i & 3], (i >> 2) & 1))) break;
+                    if (!(ok = wait(&bars->kt[i % 3], (i / 3) & 1))) break;
                     tc::tc_fence_after();
-                    const uint64_t dk = desc(sm + SM_KT + 16384u * (i & 3), 128, 1024);
+                    const uint64_t dk = desc(sm + SM_KT + 16384u * (i % 3), 128, 1024);
 #pragma unroll
                     for (int s = 0; s < C / 16; ++s)
                         tc::mma_f16_ts(tmem + T_DC, dh + 8 * s, dk + (uint64_t)(16 * s), idC, s > 0);
@@ -853,26 +864,27 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
                 constexpr uint32_t idB2 = tc::idesc_f16(128, 64, false, true); // B = P (MN-major)
                 constexpr uint32_t idB = tc::idesc_f16(128, 64);               // B = Qbar (K-major)
                 auto issue_z = [&](int m) -> bool {
-                    if (!(wait(&bars->w[m & 3], (m >> 2) & 1) && wait(&bars->kt[(m - 1) & 3], ((m - 1) >> 2) & 1) &&
+                    if (!(wait(&bars->w[m & 3], (m >> 2) & 1) && wait(&bars->kt[(m - 1) % 3], ((m - 1) / 3) & 1) &&
                           (m == 1 || wait(&bars->dz_free, (m - 2) & 1))))
                         return false;
                     tc::tc_fence_after();
                     const uint64_t dw = desc(sm + SM_W + 16384u * (m & 3), 1024, 128);
-                    const uint64_t dk = desc(sm + SM_KT + 16384u * ((m - 1) & 3), 1024, 128);
+                    const uint64_t dk = desc(sm + SM_KT + 16384u * ((m - 1) % 3), 1024, 128);
 #pragma unroll
                     for (int s = 0; s < D / 16; ++s)
                         tc::mma_f16_ss(tmem + T_DZ, dw + (uint64_t)(128 * s), dk + (uint64_t)(128 * s), idZ, s > 0);
                     tc::mma_commit(&bars->z);
                     return true;
                 };
-                const uint64_t dp = desc(sm + SM_P, 1024, 128), dq = desc(sm + SM_QB, 128, 2048);
                 ok = n < 2 || issue_z(1);
                 for (int i = 0; ok && i < n; ++i) {
                     if (i + 2 < n && !(ok = issue_z(i + 2))) break;
                     if (!(ok = wait(&bars->delta_ready[i & 1], (i >> 1) & 1) && wait(&bars->sh_ready[i & 3], (i >> 2) & 1) &&
-                               wait(&bars->qp, i & 1) && (i == 0 || wait(&bars->do_free, (i - 1) & 1))))
+                               wait(&bars->qp[i & 1], (i >> 1) & 1) && (i == 0 || wait(&bars->do_free, (i - 1) & 1))))
                         break;
                     tc::tc_fence_after();
+                    const unsigned char* qpb = sm + SM_QP + QP_SLOT * (i & 1);
+                    const uint64_t dq = desc(qpb, 128, 2048), dp = desc(qpb + QP_P, 1024, 128);
                     const uint32_t sh = tmem + T_SH + 64 * (i & 1), dh = tmem + T_DH + 32 * (i & 1);
 #pragma unroll
                     for (int s = 0; s < C / 16; ++s)   // (b2) P_i Delta_i
@@ -884,7 +896,7 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
                 }
             } else {
                 // ---- warp 18: record copies, each issued once its slot's last reader is done
-                uint64_t* const lbar0 = &bars->w[0];          // w[4], kt[4], u[2], qp: 11 load barriers
+                uint64_t* const lbar0 = &bars->w[0];          // w[4], kt[3], u[2], qp[2]: 11 load barriers
                 uint32_t uses[11] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
                 auto issue = [&](uint64_t* bar, int j, uint32_t dst, uint32_t src, uint32_t bytes, uint32_t dst2,
                                  uint32_t src2, uint32_t bytes2) {
@@ -895,28 +907,25 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
                 };
                 auto load_w = [&](int j) { issue(&bars->w[j & 3], j, SM_W + 16384u * (j & 3), HRec::W, 16384, 0, 0, 0); };
                 auto load_kt = [&](int j) {
-                    issue(&bars->kt[j & 3], j, SM_KT + 16384u * (j & 3), HRec::KT, 16384, SM_GL + 512u * (j & 3), HRec::GL, 512);
+                    issue(&bars->kt[j % 3], j, SM_KT + 16384u * (j % 3), HRec::KT, 16384, SM_GL + 512u * (j % 3), HRec::GL, 512);
                 };
                 auto load_u = [&](int j) { issue(&bars->u[j & 1], j, SM_U + 16384u * (j & 1), HRec::U, 16384, 0, 0, 0); };
-                auto load_qp = [&](int j) { issue(&bars->qp, j, SM_QB, HRec::QB, 24576, 0, 0, 0); };
+                auto load_qp = [&](int j) { issue(&bars->qp[j & 1], j, SM_QP + QP_SLOT * (j & 1), HRec::QB, QP_SLOT, 0, 0, 0); };
                 for (int j = 0; j < 4 && j < n; ++j) load_w(j);
-                for (int j = 0; j < 3 && j < n; ++j) load_kt(j);
-                for (int j = 0; j < 2 && j < n; ++j) load_u(j);
-                load_qp(0);
+                for (int j = 0; j < 2 && j < n; ++j) { load_kt(j); load_u(j); load_qp(j); }
                 for (int i = 0; ok && i < n; ++i) {
                     // Delta_i done: U_i has been read and the chain MMA of chunk i (the last reader of W_i) is done
                     if (!(ok = wait(&bars->delta_ready[i & 1], (i >> 1) & 1))) break;
                     if (i + 2 < n) load_u(i + 2);
                     if (i + 4 < n) load_w(i + 4);
-                    if (i + 1 < n) {       // the outputs of chunk i are done with Qbar and P
-                        if (!(ok = wait(&bars->o[i & 1], (i >> 1) & 1))) break;
-                        load_qp(i + 1);
-                    }
-                    if (i + 3 < n) {       // Ktil_{i-1} and gamma_{i-1}: read by (c) of i - 1, the S update
+                    if (i + 2 < n) {       // Ktil_{i-1} and gamma_{i-1}: read by (c) of i - 1, the S update
                         if (i >= 1 &&      // of i - 1 (sh_ready(i)) and Z_i / W'_i (zw_ready(i))
                             !(ok = wait(&bars->sh_ready[i & 3], (i >> 2) & 1) && wait(&bars->zw_ready[(i - 1) & 3], ((i - 1) >> 2) & 1)))
                             break;
-                        load_kt(i + 3);
+                        load_kt(i + 2);
+                        // the outputs of chunk i are done with its Qbar and P
+                        if (!(ok = wait(&bars->o[i & 1], (i >> 1) & 1))) break;
+                        load_qp(i + 2);
                     }
                 }
                 for (int bi = 0; bi < 11; ++bi)              // copies in flight land before the CTA exits (bounded)
@@ -979,11 +988,11 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
         tc::tc_fence_before();
         tc::mbar_arrive(&bars->sh_ready[0]);
         for (int j = 0; j < n; ++j) {
-            bool okw = wait(&bars->c, j & 1) && wait(&bars->kt[j & 3], (j >> 2) & 1) &&
+            bool okw = wait(&bars->c, j & 1) && wait(&bars->kt[j % 3], (j / 3) & 1) &&
                        (j < 1 || wait(&bars->o[(j - 1) & 1], ((j - 1) >> 1) & 1));
             if (!__all_sync(0xffffffffu, okw)) break;
             tc::tc_fence_after();
-            const float* gl = reinterpret_cast<const float*>(sm + SM_GL + 512u * (j & 3)) + 64 * g;
+            const float* gl = reinterpret_cast<const float*>(sm + SM_GL + 512u * (j % 3)) + 64 * g;
             const uint32_t dst = tmem + lane_base + T_SH + 64 * ((j + 1) & 1) + 32 * g;
             const bool more = j + 1 < n;
 #pragma unroll
@@ -1019,7 +1028,7 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
         auto z_epilogue = [&](int m) -> bool {
             // the Z slot m & 1 last held Z_{m-2}, read by the chain MMA of chunk m - 2
             bool okw = wait(&bars->z, (m - 1) & 1) && (m < 2 || wait(&bars->delta_ready[m & 1], ((m - 2) >> 1) & 1)) &&
-                       wait(&bars->w[m & 3], (m >> 2) & 1) && wait(&bars->kt[(m - 1) & 3], ((m - 1) >> 2) & 1);
+                       wait(&bars->w[m & 3], (m >> 2) & 1) && wait(&bars->kt[(m - 1) % 3], ((m - 1) / 3) & 1);
             if (tc::bar_any<1, 128>(!okw)) return false;   // the same exit for all four warps
             tc::tc_fence_after();
             unsigned char* zimg = sm + SM_Z + 8192u * (m & 1);
@@ -1036,7 +1045,7 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
             tc::tc_fence_before();
             tc::mbar_arrive(&bars->dz_free);
             // W'_m = W_m Diag(gamma_{m-1}), in place: 16-byte chunk f holds W[r0 .. r0 + 7][c]
-            const float* gl = reinterpret_cast<const float*>(sm + SM_GL + 512u * ((m - 1) & 3));
+            const float* gl = reinterpret_cast<const float*>(sm + SM_GL + 512u * ((m - 1) % 3));
             unsigned char* wimg = sm + SM_W + 16384u * (m & 3);
 #pragma unroll 2
             for (int f = v; f < 1024; f += 128) {
@@ -1264,14 +1273,12 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
     const int64_t ch = blockIdx.x;
     const int h = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    int64_t nch = a.seq_off[a.N];
-    if (nch > a.max_chunks) nch = a.max_chunks;
-    if (ch >= nch) return;
-    const int32_t seq = a.chunk_seq[ch];
-    const int64_t slot = a.state_idx[seq];
-    if (slot < 0 || slot >= a.num_slots) return;
-    const int64_t t0 = a.chunk_start[ch];
-    const int L = a.chunk_len[ch];
+    // one 16-byte record per chunk: {sequence, first token, length, slot}; length 0 past the last
+    // chunk, slot -1 for padding rows (the state pass writes their zero outputs)
+    const int4 info = a.chunk_info[ch];
+    if (info.z <= 0 || info.w < 0) return;
+    const int64_t t0 = info.y;
+    const int L = info.z;
     const int H = a.H;
     const float rate = expf(a.A_log[h]);
     bool tc_ok = true;                                       // thread 0: every tcgen05 wait completed
@@ -1786,8 +1793,9 @@ cudaError_t run_prefill(const kda_params& p, const GateParams& gp, const void* q
 
     cudaError_t e;
     if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
-    chunk_table_kernel<<<1, 1024, 0, stream>>>(cu, N, T, C, w.max_chunks, chunk_seq, chunk_start, chunk_len, seq_off,
-                                               seq_order);
+    int4* chunk_info = reinterpret_cast<int4*>(reinterpret_cast<char*>(workspace) + w.info_offset);
+    chunk_table_kernel<<<1, 1024, 0, stream>>>(cu, N, T, C, w.max_chunks, state_idx, num_slots, chunk_seq, chunk_start,
+                                               chunk_len, seq_off, seq_order, chunk_info);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return e;
@@ -1795,6 +1803,7 @@ cudaError_t run_prefill(const kda_params& p, const GateParams& gp, const void* q
     IntraArgs ia;
     ia.q = q; ia.k = k; ia.v = v; ia.g_raw = g_raw; ia.b_raw = b_raw; ia.A_log = A_log; ia.dt_bias = dt_bias;
     ia.chunk_seq = chunk_seq; ia.chunk_start = chunk_start; ia.chunk_len = chunk_len; ia.seq_off = seq_off;
+    ia.chunk_info = chunk_info;
     ia.state_idx = state_idx; ia.num_slots = num_slots; ia.max_chunks = w.max_chunks; ia.N = N; ia.H = H;
     ia.gp = gp; ia.ws = ws; ia.ws_stride = w.per_chunk_head;
     dim3 gi((unsigned)w.max_chunks, (unsigned)H);

@@ -415,19 +415,19 @@ recurrent_kernel(const RecArgs a)
                 pq = fmaf(e.x, qh[4 * j + 0], pq); pq = fmaf(e.y, qh[4 * j + 1], pq);
                 pq = fmaf(e.z, qh[4 * j + 2], pq); pq = fmaf(e.w, qh[4 * j + 3], pq);
             }
-#pragma unroll
-            for (int off = LPR / 2; off > 0; off >>= 1) {
-                pk += __shfl_xor_sync(0xffffffffu, pk, off);
-                pq += __shfl_xor_sync(0xffffffffu, pq, off);
-            }
-            if (decomp) {                               // + sum_j (k~_j . (a o z)) d_j[row]
+            if (decomp) {          // + sum_j (k~_j . (a o z)) d_j[row], the entries split over the row's lanes
                 const float* s_rd = s_sc + 8 * T + (size_t)a.ring_len * D;
                 const float* s_ck = s_sc + 8 * T + (size_t)3 * a.ring_len * D + D;
-                for (int j = 0; j < wp; ++j) {
+                for (int j = li; j < wp; j += LPR) {
                     const float dj = s_rd[j * D + row];
                     pk = fmaf(s_ck[j], dj, pk);
                     pq = fmaf(s_ck[a.ring_len + j], dj, pq);
                 }
+            }
+#pragma unroll
+            for (int off = LPR / 2; off > 0; off >>= 1) {
+                pk += __shfl_xor_sync(0xffffffffu, pk, off);
+                pq += __shfl_xor_sync(0xffffffffu, pq, off);
             }
             const float delta = beta * (vj - pk);
             const float o = fmaf(delta, qk, pq);

@@ -39,9 +39,10 @@ class Model:
     def __init__(self, n, seed, single_delta_barrier=False):
         self.n, self.rng = n, random.Random(seed)
         self.w = [Bar(f"w{i}") for i in range(4)]
-        self.kt = [Bar(f"kt{i}") for i in range(4)]
+        self.kt = [Bar(f"kt{i}") for i in range(3)]
         self.u = [Bar(f"u{i}") for i in range(2)]
-        self.qp, self.chain, self.c, self.z = Bar("qp"), Bar("chain"), Bar("c"), Bar("z")
+        self.qp = [Bar("qp0"), Bar("qp1")]
+        self.chain, self.c, self.z = Bar("chain"), Bar("c"), Bar("z")
         self.o = [Bar("o0"), Bar("o1")]
         if single_delta_barrier:        # the variant with one Delta-ready barrier: must be caught
             d = Bar("delta", 128)
@@ -107,8 +108,8 @@ def chain_and_c_issuer(M):            # warp 16
             M.mma(0, [(f"SH{i & 1}", f"S{i}"), (f"W{(i + 1) & 3}", f"W'{i + 1}"), (f"DH{i & 1}", f"D{i}"),
                       (f"Z{(i + 1) & 1}", f"Z{i + 1}")], [("DA", f"A{i + 1}")])
             M.commit(0, M.chain)
-        yield ring(M.kt, i, 4)
-        M.mma(0, [(f"DH{i & 1}", f"D{i}"), (f"KT{i & 3}", f"K{i}")], [("DC", f"C{i}")])
+        yield ring(M.kt, i, 3)
+        M.mma(0, [(f"DH{i & 1}", f"D{i}"), (f"KT{i % 3}", f"K{i}")], [("DC", f"C{i}")])
         M.commit(0, M.c)
 
 
@@ -117,10 +118,10 @@ def z_and_output_issuer(M):           # warp 17
 
     def issue_z(m):
         yield ring(M.w, m, 4)
-        yield ring(M.kt, m - 1, 4)
+        yield ring(M.kt, m - 1, 3)
         if m >= 2:
             yield single(M.dz_free, m - 2)
-        M.mma(1, [(f"W{m & 3}", f"W{m}"), (f"KT{(m - 1) & 3}", f"K{m - 1}")], [("DZ", f"Z{m}")])
+        M.mma(1, [(f"W{m & 3}", f"W{m}"), (f"KT{(m - 1) % 3}", f"K{m - 1}")], [("DZ", f"Z{m}")])
         M.commit(1, M.z)
 
     if n >= 2:
@@ -130,10 +131,10 @@ def z_and_output_issuer(M):           # warp 17
             yield from issue_z(i + 2)
         yield M.delta_wait(i)
         yield ring(M.sh, i, 4)
-        yield single(M.qp, i)
+        yield ring(M.qp, i, 2)
         if i >= 1:
             yield single(M.do_free, i - 1)
-        M.mma(1, [(f"DH{i & 1}", f"D{i}"), (f"SH{i & 1}", f"S{i}"), ("QP", f"QP{i}")], [("DO", f"O{i}")])
+        M.mma(1, [(f"DH{i & 1}", f"D{i}"), (f"SH{i & 1}", f"S{i}"), (f"QP{i & 1}", f"QP{i}")], [("DO", f"O{i}")])
         M.commit(1, M.o[i & 1])
 
 
@@ -141,31 +142,30 @@ def copy_warp(M):                     # warp 18
     n = M.n
 
     def w(j): M.copy({f"W{j & 3}": f"W{j}"}, M.w[j & 3])
-    def kt(j): M.copy({f"KT{j & 3}": f"K{j}", f"G{j & 3}": f"G{j}"}, M.kt[j & 3])
+    def kt(j): M.copy({f"KT{j % 3}": f"K{j}", f"G{j % 3}": f"G{j}"}, M.kt[j % 3])
     def u(j): M.copy({f"U{j & 1}": f"U{j}"}, M.u[j & 1])
-    def qp(j): M.copy({"QP": f"QP{j}"}, M.qp)
+    def qp(j): M.copy({f"QP{j & 1}": f"QP{j}"}, M.qp[j & 1])
 
     for j in range(min(4, n)):
         w(j)
-    for j in range(min(3, n)):
-        kt(j)
     for j in range(min(2, n)):
+        kt(j)
         u(j)
-    qp(0)
+        qp(j)
     for i in range(n):
         yield M.delta_wait(i)
         if i + 2 < n:
             u(i + 2)
         if i + 4 < n:
             w(i + 4)
-        if i + 1 < n:
-            yield ring(M.o, i, 2)
-            qp(i + 1)
-        if i + 3 < n:
+        if i + 2 < n:
             if i >= 1:
                 yield ring(M.sh, i, 4)
                 yield ring(M.zw, i - 1, 4)
-            kt(i + 3)
+            kt(i + 2)
+        if i + 2 < n:
+            yield ring(M.o, i, 2)
+            qp(i + 2)
 
 
 def delta_pass(M):                    # warps 0..3
@@ -185,11 +185,11 @@ def state_update(M):                  # warps 4..11
     M.sh[0].arrive(256)
     for j in range(M.n):
         yield single(M.c, j)
-        yield ring(M.kt, j, 4)
+        yield ring(M.kt, j, 3)
         if j >= 1:
             yield ring(M.o, j - 1, 2)
         M.read("DC", f"C{j}", "S update")
-        M.read(f"G{j & 3}", f"G{j}", "S update")
+        M.read(f"G{j % 3}", f"G{j}", "S update")
         if j + 1 < M.n:
             M.write(f"SH{(j + 1) & 1}", f"S{j + 1}")
         M.sh[(j + 1) & 3].arrive(256)
@@ -203,12 +203,12 @@ def z_w_output_warps(M):              # warps 12..15
         if m >= 2:
             yield M.delta_wait(m - 2)            # the Z slot's previous reader, chain MMA m - 2, is done
         yield ring(M.w, m, 4)
-        yield ring(M.kt, m - 1, 4)
+        yield ring(M.kt, m - 1, 3)
         M.read("DZ", f"Z{m}", "Z epilogue")
         M.write(f"Z{m & 1}", f"Z{m}")
         M.dz_free.arrive(128)
         M.read(f"W{m & 3}", f"W{m}", "W' scaling")
-        M.read(f"G{(m - 1) & 3}", f"G{m - 1}", "W' scaling")
+        M.read(f"G{(m - 1) % 3}", f"G{m - 1}", "W' scaling")
         M.write(f"W{m & 3}", f"W'{m}")
         M.zw[(m - 1) & 3].arrive(128)
 
