@@ -30,8 +30,10 @@
 //     running product is accumulated token by token.
 // Products of factors in (0, 1] cannot overflow and lose at most one rounding per factor, so the
 // fp32 path keeps the 1e-5 relative accuracy the fp32 configuration needs.
+#include <cuda.h>          // CUtensorMap and its encoder's types (the encoder is fetched at run time)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include <type_traits>
@@ -1229,8 +1231,8 @@ constexpr uint32_t OFF_BP = OFF_AD + NB * 256 * 4;   // block products bp      [
 constexpr uint32_t OFF_EB = OFF_BP + NB * D * 4;     // e^{G} before block b: prod_{b' < b} bp  [NB][D]
 constexpr uint32_t OFF_B12 = OFF_EB + NB * D * 4;    // bp[1] * bp[2]          [D]
 constexpr uint32_t OFF_BETA = OFF_B12 + D * 4;       // beta                   [C]
-constexpr uint32_t OFF_BAR = OFF_BETA + C * 4;       // 3 mbarriers: Gram done, U/W done, drain
-constexpr uint32_t OFF_TM = OFF_BAR + 24;            // TMEM base
+constexpr uint32_t OFF_BAR = OFF_BETA + C * 4;       // 4 mbarriers: Gram done, U/W done, drain, inputs landed
+constexpr uint32_t OFF_TM = OFF_BAR + 32;            // TMEM base
 constexpr uint32_t BYTES = OFF_TM + 16;
 constexpr uint32_t OFF_A = OFF_K;                    // A = sum of diagonal and Gram blocks [C][LDA]
 constexpr uint32_t OFF_X = OFF_K + C * LDA * 4;      // 3 scratch 16 x 16 blocks
@@ -1247,7 +1249,11 @@ constexpr uint32_t T_KB = 64;     // (beta Kbar)^T (64)
 constexpr uint32_t T_G = 128;     // Gram result (96); then U^T (64) and W^T (64)
 }  // namespace itc
 
-__global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const IntraArgs a)
+// The chunk's k, q (bf16) and g (fp32) tiles arrive by tensor-map copies (cp.async.bulk.tensor) issued
+// by thread 0 at entry: raw k and q into the q tile, raw g into the alpha tile, dense [64][128].
+__global__ void __launch_bounds__(itc::THREADS, 2)
+chunk_intra_tc_kernel(const IntraArgs a, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_g)
 {
     using namespace itc;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -1268,6 +1274,7 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
     uint64_t* bar_g = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     uint64_t* bar_uw = bar_g + 1;
     uint64_t* bar_drain = bar_g + 2;
+    uint64_t* bar_in = bar_g + 3;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + OFF_TM);
 
     const int64_t ch = blockIdx.x;
@@ -1282,58 +1289,68 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
     const int H = a.H;
     const float rate = expf(a.A_log[h]);
     bool tc_ok = true;                                       // thread 0: every tcgen05 wait completed
-    const __nv_bfloat16* kp = reinterpret_cast<const __nv_bfloat16*>(a.k);
-    const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(a.q);
     const __nv_bfloat16* vp = reinterpret_cast<const __nv_bfloat16*>(a.v);
 
     // record fields, addressed from one base pointer where they are written
     unsigned char* const rec = reinterpret_cast<unsigned char*>(a.ws + ((size_t)ch * H + h) * a.ws_stride);
 #define KDA_REC(field) (rec + HRec::field)
 
-    if (warp == 0) {
-        tc::tmem_alloc(s_tmem, 256);
-        tc::tmem_relinquish();
-    }
-    if (tid == 0) {
+    if (tid == 0) {               // the input tiles first: everything below overlaps their latency
         tc::mbar_init(bar_g, 1);
         tc::mbar_init(bar_uw, 1);
         tc::mbar_init(bar_drain, 1);
+        tc::mbar_init(bar_in, 1);
         tc::fence_mbar_init();
+        tc::mbar_arrive_expect_tx(bar_in, 2 * C * D * 2 + C * D * 4);
+        tc::tma_load_2d(sm + OFF_Q, &tm_k, h * D, (int32_t)t0, bar_in);
+        tc::tma_load_2d(sm + OFF_Q + C * D * 2, &tm_q, h * D, (int32_t)t0, bar_in);
+        tc::tma_load_2d(sm + OFF_AL, &tm_g, h * D, (int32_t)t0, bar_in);
+    }
+    __syncthreads();              // the barriers are initialised before any thread waits on them
+    if (warp == 0) {
+        tc::tmem_alloc(s_tmem, 256);
+        tc::tmem_relinquish();
     }
     if (warp == 1) {               // the value rows are read after the Gram: start them towards L2 now
         for (int r = lane; r < L; r += 32)
             asm volatile("cp.async.bulk.prefetch.L2.global [%0], 256;" ::"l"(vp + ((size_t)(t0 + r) * H + h) * D)
                          : "memory");
     }
-    // 1. loads, all issued before any is used (rows past the chunk end: k = q = 0, alpha = 1,
-    //    beta = 0).  k, q: 8 elements in rows 2 warp + (lane bit 2) + 16 i, columns 32 (lane >> 3) +
-    //    8 (lane & 3): the two 8-lane halves of a quarter-warp hold adjacent rows, so that with the
-    //    132-float row stride each 16-byte shared store of a quarter-warp covers all 32 banks once.
-    //    g: 4 elements in rows (tid >> 5) + 8 i
+    // 1. the staged tiles to registers (rows past the chunk end, another sequence's or zero-filled
+    //    past T: k = q = 0, alpha = 1, beta = 0), then the tiles are rewritten in place.  k, q: 8
+    //    elements in rows 2 warp + (lane bit 2) + 16 i, columns 32 (lane >> 3) + 8 (lane & 3): the
+    //    two 8-lane halves of a quarter-warp hold adjacent rows, so that with the 132-float row stride
+    //    each 16-byte shared store of a quarter-warp covers all 32 banks once.  g: 4 elements in rows
+    //    (tid >> 5) + 8 i
     {
+        float bt = 0.f;
+        if (tid < L) bt = a.b_raw[(size_t)(t0 + tid) * H + h];
+        const int c4 = (tid & 31) * 4;
+        float4 db = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a.dt_bias) db = *reinterpret_cast<const float4*>(a.dt_bias + (size_t)h * D + c4);
+        const bool landed = tc::mbar_wait(bar_in, 0, kWaitPolls);
+        if (!landed && tid == 0) record_error(kDevErrTimeout);
+        if (tid == 0) tc_ok = tc_ok && landed;
         uint4 kv[4], qv[4];
         float4 gv[8];
+        const unsigned char* rawk = sm + OFF_Q;
+        const unsigned char* rawq = sm + OFF_Q + C * D * 2;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int r = 2 * warp + ((lane >> 2) & 1) + 16 * i, c8 = 32 * (lane >> 3) + 8 * (lane & 3);
             kv[i] = qv[i] = make_uint4(0, 0, 0, 0);
             if (r < L) {
-                const size_t idx = ((size_t)(t0 + r) * H + h) * D + c8;
-                kv[i] = *reinterpret_cast<const uint4*>(kp + idx);
-                qv[i] = *reinterpret_cast<const uint4*>(qp + idx);
+                kv[i] = *reinterpret_cast<const uint4*>(rawk + (r * D + c8) * 2);
+                qv[i] = *reinterpret_cast<const uint4*>(rawq + (r * D + c8) * 2);
             }
         }
-        const int c4 = (tid & 31) * 4;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int r = (tid >> 5) + 8 * i;
             gv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (r < L) gv[i] = *reinterpret_cast<const float4*>(a.g_raw + ((size_t)(t0 + r) * H + h) * D + c4);
+            if (r < L) gv[i] = ld4(reinterpret_cast<const float*>(sm + OFF_AL) + r * D + c4);
         }
-        float bt = 0.f;
-        if (tid < L) bt = a.b_raw[(size_t)(t0 + tid) * H + h];
-        float4 db = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (a.dt_bias) db = *reinterpret_cast<const float4*>(a.dt_bias + (size_t)h * D + c4);
+        __syncthreads();          // every raw value is in registers before the tiles are rewritten
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             // the 16 lanes that hold row r (lane bit 2 fixed) reduce its squared norms with shuffles
@@ -1770,6 +1787,36 @@ __global__ void __launch_bounds__(itc::THREADS, 2) chunk_intra_tc_kernel(const I
 }
 
 // ---- host-side dispatch --------------------------------------------------------------------------
+// cuTensorMapEncodeTiled, fetched from the driver once (no link to the driver library is needed).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// A [rows][cols] row-major tensor (element size esz bytes) read in boxes of box_rows x box_cols,
+// no swizzle, zero fill outside the tensor.
+cudaError_t encode_rows_x_cols(CUtensorMap* m, CUtensorMapDataType type, const void* base, int64_t rows,
+                               uint64_t cols, uint32_t esz, uint32_t box_cols, uint32_t box_rows)
+{
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)(cols * esz)};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(m, type, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int C, int D, typename TIn, typename TOut>
 cudaError_t run_prefill(const kda_params& p, const GateParams& gp, const void* q, const void* k,
                         const void* v, const float* g_raw, const float* b_raw, const float* A_log,
@@ -1808,12 +1855,18 @@ cudaError_t run_prefill(const kda_params& p, const GateParams& gp, const void* q
     ia.gp = gp; ia.ws = ws; ia.ws_stride = w.per_chunk_head;
     dim3 gi((unsigned)w.max_chunks, (unsigned)H);
     if constexpr (kTensorCore) {
+        // tensor maps of k, q (bf16) and g (fp32) as 2D tensors [T][H * D], 64 x 128 boxes
+        CUtensorMap tm[3];
+        e = encode_rows_x_cols(&tm[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k, T, (uint64_t)H * D, 2, D, C);
+        if (e == cudaSuccess) e = encode_rows_x_cols(&tm[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, T, (uint64_t)H * D, 2, D, C);
+        if (e == cudaSuccess) e = encode_rows_x_cols(&tm[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, g_raw, T, (uint64_t)H * D, 4, D, C);
+        if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(chunk_intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)itc::BYTES);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(chunk_intra_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
-        chunk_intra_tc_kernel<<<gi, itc::THREADS, itc::BYTES, stream>>>(ia);
+        chunk_intra_tc_kernel<<<gi, itc::THREADS, itc::BYTES, stream>>>(ia, tm[0], tm[1], tm[2]);
     } else {
         using IS = IntraShape<C, D>;
         auto intra = chunk_intra_kernel<C, D, TIn>;

@@ -139,6 +139,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// ---- tensor (tiled) bulk copy global -> shared through a tensor map ----------------------------------
+// 2D box at element coordinates (x = innermost, y); x * element size must be a multiple of 16 bytes.
+// Elements outside the tensor read as zero.  tmap is the address of a CUtensorMap kernel parameter
+// (__grid_constant__).  Completion is signalled on the mbarrier as transaction bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t x, int32_t y, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ---- bulk async copy shared -> global (bulk-group completion) -------------------------------------
 // src and dst 16-byte aligned, bytes a multiple of 16.  The issuing thread tracks completion with
 // bulk_commit / bulk_wait_read (the shared source may be reused) / bulk_wait (writes done).
