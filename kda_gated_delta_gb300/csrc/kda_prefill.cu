@@ -1371,7 +1371,7 @@ chunk_intra_tc_kernel(const IntraArgs a, const __grid_constant__ CUtensorMap tm_
                 kk += __shfl_xor_sync(0xffffffffu, kk, off);
                 qq += __shfl_xor_sync(0xffffffffu, qq, off);
             }
-            const float rk = 1.0f / sqrtf(kk + a.gp.l2_eps), rq = a.gp.scale / sqrtf(qq + a.gp.l2_eps);
+            const float rk = rsqrtf(kk + a.gp.l2_eps), rq = a.gp.scale * rsqrtf(qq + a.gp.l2_eps);
 #pragma unroll
             for (int t = 0; t < 8; ++t) { kf[t] *= rk; qf[t] *= rq; }
             st4(sK + r * LD + c8, make_float4(kf[0], kf[1], kf[2], kf[3]));
