@@ -41,24 +41,34 @@ UNIT = "tokens/s"
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, one ncu capture of a bench
-# step, caches flushed before each kernel), valid only for the kernel source they were taken on.
+# step, caches flushed before each kernel), valid only for the kernel source they were taken on:
+# the hash covers the kernel's file and the two headers every kernel file includes.
 MEASURED_TRAFFIC = {
-    "kda_prefill.cu": {"sha256_16": "c45683e980ef8a5c",
-                       "kda_chunk_table": 0.0, "kda_chunk_intra": 1869.7e6, "kda_chunk_state": 1393.3e6},
-    "kda_recurrent.cu": {"sha256_16": "302ea2e2dab4d254",
-                         "kda_recurrent_decode": 1024.6e6, "kda_recurrent_verify": 614.1e6,
-                         "kda_replay_decode": 620.5e6},
+    "kda_prefill.cu": {"sha256_16": "70923e2c089a3ec5",
+                       "kda_chunk_table": 0.02e6, "kda_chunk_intra": 1257.7e6, "kda_chunk_state": 761.1e6},
+    "kda_recurrent.cu": {"sha256_16": "55b03304299d9b86",
+                         "kda_recurrent_decode": 1022.1e6, "kda_recurrent_verify": 614.3e6,
+                         "kda_replay_decode_l8": 623.5e6, "kda_replay_decode_l16": 662.6e6},
 }
+TRAFFIC_HEADERS = ("kda_internal.cuh", "kda_tc.cuh")
+
+
+def source_hash(src):
+    """First 16 hex digits of the sha256 of a kernel file followed by the shared headers."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in (src,) + TRAFFIC_HEADERS:
+        with open(os.path.join(ROOT, "kda_gated_delta_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def measured_traffic(kernel):
     """Bytes per launch from the stored capture, or None if the kernel's source changed since."""
-    import hashlib
     for src, rec in MEASURED_TRAFFIC.items():
         if kernel in rec:
-            path = os.path.join(ROOT, "kda_gated_delta_gb300", "csrc", src)
             try:
-                h = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+                h = source_hash(src)
             except OSError:
                 return None
             return rec[kernel] if h == rec["sha256_16"] else None
@@ -638,6 +648,68 @@ def run_ours(args):
     return 0
 
 
+def run_decode_only(args):
+    """--only decode: the decode, verify and buffered-decode kernels on their workloads, without the
+    prefill workload, so that a profiler capture of them holds a few GB instead of eight.  Prints one
+    JSON line with each kernel's time and roofline fraction (a profiling aid, not the bench line)."""
+    import torch
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    from kda_gated_delta_gb300 import build as kbuild
+    kbuild.build()
+    import kda_gated_delta_gb300 as kda
+    from kda_gated_delta_gb300 import workloads
+
+    bw_peak, _, _ = peaks()
+    H, D = 32, 128
+    wd, wv = workloads.workload(2), workloads.workload(4)
+    dec = workloads.to_device(workloads.workload_inputs(2), dev)
+    ver = workloads.to_device(workloads.workload_inputs(4), dev)
+    p_dec = kda.make_params(H, D, io_dtype=torch.bfloat16, out_dtype=torch.bfloat16)
+    p_ver = kda.make_params(H, D, io_dtype=torch.bfloat16, out_dtype=torch.bfloat16, gate="gdn")
+    out_dec = torch.empty(wd.batch, H, D, dtype=torch.bfloat16, device=dev)
+    out_ver = torch.empty(wv.batch * wv.t_draft, H, D, dtype=torch.bfloat16, device=dev)
+    inter = torch.empty(wv.batch, wv.t_draft, H, D, D, dtype=torch.float32, device=dev)
+    RL = 8
+    rpool = dec["pool"].clone()
+    rings = kda.replay_rings(rpool.shape[0], H, D, RL, device=dev)
+    pos = [torch.tensor([(t + b) % RL for b in range(wd.batch)], dtype=torch.int32, device=dev) for t in range(RL)]
+    out_rep = torch.empty(wd.batch, H, D, dtype=torch.bfloat16, device=dev)
+    K, W = args.steps, args.warmup
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K + W)]
+
+    def step(i):
+        ev[i][0].record()
+        kda.recurrent_decode(dec["q"], dec["k"], dec["v"], dec["g_raw"], dec["b_raw"], dec["A_log"],
+                             dec["dt_bias"], dec["pool"], dec["state_idx"], out_dec, params=p_dec)
+        ev[i][1].record()
+        kda.recurrent_verify(ver["q"], ver["k"], ver["v"], ver["g_raw"], ver["b_raw"], ver["A_log"],
+                             ver["dt_bias"], ver["pool"], ver["state_idx"], wv.t_draft, inter, out_ver, params=p_ver)
+        ev[i][2].record()
+        kda.replay_decode(dec["q"], dec["k"], dec["v"], dec["g_raw"], dec["b_raw"], dec["A_log"],
+                          dec["dt_bias"], rpool, dec["state_idx"], rings, pos[i % RL], None, out_rep, params=p_dec)
+        ev[i][3].record()
+
+    for i in range(W):
+        step(K + i)
+    torch.cuda.synchronize()
+    for i in range(K):
+        step(i)
+    torch.cuda.synchronize()
+    if kda.check_device_errors() != 0:
+        raise RuntimeError("device error recorded")
+    ms = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) / K for j in range(3)]
+    byts = (decode_bytes(wd.batch, H, D, 2, 2), verify_bytes(wv.batch, wv.t_draft, H, D, 2, 2),
+            sum(replay_bytes(pos[i % RL].tolist(), RL, H, D, 2, 2) for i in range(K)) / K)
+    line = {"mode": "decode only (profiling aid)", "steps": K, "warmup": W,
+            "kernels": [{"name": n, "ms": round(m, 5), "hbm_frac": round(b / (m * 1e-3) / 1e9 / bw_peak, 4)}
+                        for n, m, b in zip(("kda_recurrent_decode", "kda_recurrent_verify", "kda_replay_decode_l8"),
+                                           ms, byts)]}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -646,13 +718,16 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default="all", choices=["all", "prefill"],
-                    help="prefill: the varlen prefill alone, for profiler captures")
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
+                    help="prefill: the varlen prefill alone; decode: decode, verify and buffered decode alone "
+                         "(both for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.only == "decode":
+        return run_decode_only(args)
     return run_ours(args)
 
 
