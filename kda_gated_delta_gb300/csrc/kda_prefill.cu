@@ -702,6 +702,7 @@ constexpr uint32_t SM_MISC = SM_BAR + 256;
 constexpr uint32_t SM_OUT = SM_MISC + 64;   // 16384: output rows staged for the 16-byte stores
 constexpr uint32_t BYTES = SM_OUT + 16384;
 constexpr int THREADS = 608;
+constexpr int kPrefetchAhead = 4;       // records prefetched into L2 this many chunks ahead
 static_assert(SM_KT + 3 * 16384 == SM_U && SM_U + 2 * 16384 == SM_QP && SM_QP + 2 * QP_SLOT == SM_Z &&
               SM_Z + 2 * 8192 == SM_GL && SM_GL + 3 * 512 <= SM_BAR, "layout");
 static_assert(BYTES <= 232448, "state-pass shared memory");
@@ -843,10 +844,10 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
                         const uint32_t sh = tmem + T_SH + 64 * (i & 1);
                         const uint64_t dw = desc(sm + SM_W + 16384u * ((i + 1) & 3), 1024, 128);
                         const uint64_t dz = desc(sm + SM_Z + 8192u * ((i + 1) & 1), 128, 1024);
-#pragma unroll
+#pragma unroll 1
                         for (int s = 0; s < D / 16; ++s)      // descriptor start advances in 16-byte units
                             tc::mma_f16_ts(tmem + T_DA, sh + 8 * s, dw + (uint64_t)(128 * s), idChainS, s > 0);
-#pragma unroll
+#pragma unroll 1
                         for (int s = 0; s < C / 16; ++s)
                             tc::mma_f16_ts(tmem + T_DA, dh + 8 * s, dz + (uint64_t)(16 * s), idChainZ, 1);
                         tc::mma_commit(&bars->chain);
@@ -855,7 +856,7 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
                     if (!(ok = wait(&bars->kt[i % 3], (i / 3) & 1))) break;
                     tc::tc_fence_after();
                     const uint64_t dk = desc(sm + SM_KT + 16384u * (i % 3), 128, 1024);
-#pragma unroll
+#pragma unroll 1
                     for (int s = 0; s < C / 16; ++s)
                         tc::mma_f16_ts(tmem + T_DC, dh + 8 * s, dk + (uint64_t)(16 * s), idC, s > 0);
                     tc::mma_commit(&bars->c);
@@ -872,7 +873,7 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
                     tc::tc_fence_after();
                     const uint64_t dw = desc(sm + SM_W + 16384u * (m & 3), 1024, 128);
                     const uint64_t dk = desc(sm + SM_KT + 16384u * ((m - 1) % 3), 1024, 128);
-#pragma unroll
+#pragma unroll 1
                     for (int s = 0; s < D / 16; ++s)
                         tc::mma_f16_ss(tmem + T_DZ, dw + (uint64_t)(128 * s), dk + (uint64_t)(128 * s), idZ, s > 0);
                     tc::mma_commit(&bars->z);
@@ -888,34 +889,38 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
                     const unsigned char* qpb = sm + SM_QP + QP_SLOT * (i & 1);
                     const uint64_t dq = desc(qpb, 128, 2048), dp = desc(qpb + QP_P, 1024, 128);
                     const uint32_t sh = tmem + T_SH + 64 * (i & 1), dh = tmem + T_DH + 32 * (i & 1);
-#pragma unroll
+#pragma unroll 1
                     for (int s = 0; s < C / 16; ++s)   // (b2) P_i Delta_i
                         tc::mma_f16_ts(tmem + T_DO, dh + 8 * s, dp + (uint64_t)(128 * s), idB2, s > 0);
-#pragma unroll
+#pragma unroll 1
                     for (int s = 0; s < D / 16; ++s)   // (b) + Qbar_i S_i
                         tc::mma_f16_ts(tmem + T_DO, sh + 8 * s, dq + (uint64_t)(16 * s), idB, 1);
                     tc::mma_commit(&bars->o[i & 1]);
                 }
             } else {
                 // ---- warp 18: record copies, each issued once its slot's last reader is done
-                uint64_t* const lbar0 = &bars->w[0];          // w[4], kt[3], u[2], qp[2]: 11 load barriers
-                uint32_t uses[11] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+                // Each kind is copied for chunks 0, 1, 2, ... in order; n_x counts the copies issued.
+                int n_w = 0, n_kt = 0, n_u = 0, n_qp = 0;
                 auto issue = [&](uint64_t* bar, int j, uint32_t dst, uint32_t src, uint32_t bytes, uint32_t dst2,
                                  uint32_t src2, uint32_t bytes2) {
-                    ++uses[bar - lbar0];
                     tc::mbar_arrive_expect_tx(bar, bytes + bytes2);
                     tc::bulk_g2s(sm + dst, rec_of(j) + src, bytes, bar);
                     if (bytes2) tc::bulk_g2s(sm + dst2, rec_of(j) + src2, bytes2, bar);
                 };
-                auto load_w = [&](int j) { issue(&bars->w[j & 3], j, SM_W + 16384u * (j & 3), HRec::W, 16384, 0, 0, 0); };
+                auto load_w = [&](int j) { ++n_w; issue(&bars->w[j & 3], j, SM_W + 16384u * (j & 3), HRec::W, 16384, 0, 0, 0); };
                 auto load_kt = [&](int j) {
+                    ++n_kt;
                     issue(&bars->kt[j % 3], j, SM_KT + 16384u * (j % 3), HRec::KT, 16384, SM_GL + 512u * (j % 3), HRec::GL, 512);
                 };
-                auto load_u = [&](int j) { issue(&bars->u[j & 1], j, SM_U + 16384u * (j & 1), HRec::U, 16384, 0, 0, 0); };
-                auto load_qp = [&](int j) { issue(&bars->qp[j & 1], j, SM_QP + QP_SLOT * (j & 1), HRec::QB, QP_SLOT, 0, 0, 0); };
+                auto load_u = [&](int j) { ++n_u; issue(&bars->u[j & 1], j, SM_U + 16384u * (j & 1), HRec::U, 16384, 0, 0, 0); };
+                auto load_qp = [&](int j) { ++n_qp; issue(&bars->qp[j & 1], j, SM_QP + QP_SLOT * (j & 1), HRec::QB, QP_SLOT, 0, 0, 0); };
                 for (int j = 0; j < 4 && j < n; ++j) load_w(j);
                 for (int j = 0; j < 2 && j < n; ++j) { load_kt(j); load_u(j); load_qp(j); }
+                // Whole records are pulled into L2 kPrefetchAhead chunks ahead, so that the copies into
+                // shared memory, issued one or two chunks ahead, find them there while every SM streams.
+                for (int j = 2; j < kPrefetchAhead && j < n; ++j) tc::bulk_prefetch_l2(rec_of(j), HRec::BYTES);
                 for (int i = 0; ok && i < n; ++i) {
+                    if (i + kPrefetchAhead < n) tc::bulk_prefetch_l2(rec_of(i + kPrefetchAhead), HRec::BYTES);
                     // Delta_i done: U_i has been read and the chain MMA of chunk i (the last reader of W_i) is done
                     if (!(ok = wait(&bars->delta_ready[i & 1], (i >> 1) & 1))) break;
                     if (i + 2 < n) load_u(i + 2);
@@ -930,8 +935,15 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
                         load_qp(i + 2);
                     }
                 }
-                for (int bi = 0; bi < 11; ++bi)              // copies in flight land before the CTA exits (bounded)
-                    if (uses[bi]) tc::mbar_wait(lbar0 + bi, (uses[bi] - 1) & 1u, kWaitPolls);
+                // copies in flight land before the CTA exits (bounded): slot s of a ring of depth R last
+                // received chunk s + R ((N - 1 - s) / R) of the N copied, its phase (N - 1 - s) / R
+                auto drain = [&](uint64_t* ring, int R, int N) {
+                    for (int s = 0; s < R && s < N; ++s) tc::mbar_wait(ring + s, (uint32_t)((N - 1 - s) / R) & 1u, kWaitPolls);
+                };
+                drain(bars->w, 4, n_w);
+                drain(bars->kt, 3, n_kt);
+                drain(bars->u, 2, n_u);
+                drain(bars->qp, 2, n_qp);
             }
             if (me < 2) {           // this issuer's MMAs complete before TMEM is freed (bounded)
                 tc::mma_commit(&bars->drain[me]);
@@ -950,7 +962,7 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
             tc::tc_fence_after();
             const unsigned char* ub = sm + SM_U + 16384u * (j & 1);
             const uint32_t dst = tmem + lane_base + T_DH + 32 * (j & 1);
-#pragma unroll
+#pragma unroll 1
             for (int r0 = 0; r0 < C; r0 += 16) {
                 float d[16];
                 tc::tmem_ld16(tmem + lane_base + T_DA + r0, d);
@@ -1002,7 +1014,13 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
                 float d[16];
                 tc::tmem_ld16(tmem + lane_base + T_DC + 64 * g + c0, d);
 #pragma unroll
-                for (int t = 0; t < 16; ++t) S[c0 + t] = fmaf(S[c0 + t], gl[c0 + t], d[t]);
+                for (int t = 0; t < 16; t += 4) {
+                    const float4 gm = *reinterpret_cast<const float4*>(gl + c0 + t);
+                    S[c0 + t] = fmaf(S[c0 + t], gm.x, d[t]);
+                    S[c0 + t + 1] = fmaf(S[c0 + t + 1], gm.y, d[t + 1]);
+                    S[c0 + t + 2] = fmaf(S[c0 + t + 2], gm.z, d[t + 2]);
+                    S[c0 + t + 3] = fmaf(S[c0 + t + 3], gm.w, d[t + 3]);
+                }
                 if (more) {
                     uint32_t pk[8];
 #pragma unroll
@@ -1035,7 +1053,7 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
             tc::tc_fence_after();
             unsigned char* zimg = sm + SM_Z + 8192u * (m & 1);
             const uint32_t rp = 16 * q + (lane & 15);   // the row r' of Z this lane holds (lanes 0..15)
-#pragma unroll
+#pragma unroll 1
             for (int c0 = 0; c0 < C; c0 += 16) {
                 float d[16];
                 tc::tmem_ld16(tmem + lane_base + T_DZ + c0, d);
@@ -1049,7 +1067,7 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
             // W'_m = W_m Diag(gamma_{m-1}), in place: 16-byte chunk f holds W[r0 .. r0 + 7][c]
             const float* gl = reinterpret_cast<const float*>(sm + SM_GL + 512u * ((m - 1) % 3));
             unsigned char* wimg = sm + SM_W + 16384u * (m & 3);
-#pragma unroll 2
+#pragma unroll 1
             for (int f = v; f < 1024; f += 128) {
                 const float gm = gl[((f >> 6) << 3) + (f & 7)];
                 uint4 x = *reinterpret_cast<const uint4*>(wimg + 16 * f);
@@ -1082,7 +1100,7 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
 #pragma unroll
             for (int rb = 0; rb < C; rb += RH) {
                 if (rb > 0) tc::bar_sync<1, 128>();
-#pragma unroll
+#pragma unroll 1
                 for (int r0 = rb; r0 < rb + RH; r0 += 16) {
                     float o[16];
                     tc::tmem_ld16(tmem + lane_base + T_DO + r0, o);
@@ -1094,7 +1112,7 @@ __global__ void __launch_bounds__(stc::THREADS, 1) chunk_state_tc_kernel(const S
                     tc::mbar_arrive(&bars->do_free);
                 }
                 tc::bar_sync<1, 128>();
-#pragma unroll
+#pragma unroll 1
                 for (int pc = v; pc < RH * PIECES_PER_ROW; pc += 128) {
                     const int r = rb + pc / PIECES_PER_ROW, q16 = pc % PIECES_PER_ROW;
                     if (r < L)
@@ -1498,6 +1516,9 @@ chunk_intra_tc_kernel(const IntraArgs a, const __grid_constant__ CUtensorMap tm_
             reinterpret_cast<float*>(KDA_REC(GL))[c] = ((bp[0] * bp[1]) * bp[2]) * bp[3];
             sB12[c] = bp[1] * bp[2];
         }
+        // Both threads of column c have read all 64 alpha rows before either overwrites its two
+        // blocks of the alpha tile with k o Rout below (the two threads sit in different warps).
+        __syncthreads();
 #pragma unroll
         for (int bi = 0; bi < 2; ++bi) {
             const int blk = 2 * hf + bi;

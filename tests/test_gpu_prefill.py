@@ -2,9 +2,9 @@
 workload, edge shapes (single tokens, chunk-boundary lengths, ragged varlen, padding rows,
 empty sequences), gate extremes on both kernel pairs (decays from ~1e-3 per token to underflow,
 and g_raw + dt_bias above the softplus threshold of 20), the full varlen workload, the long
-prefill split into 32 calls carrying the state (all heads, every call), and the mode invariances
+prefill split into 32 calls carrying the state (all heads, every call), the mode invariances
 (prefill then decode equals one prefill; chunked calls equal one call; packed varlen equals
-separate calls).  The full workloads are also checked per (sequence, head), each block normalised
+separate calls) and bitwise repeatability of repeated calls.  The full workloads are also checked per (sequence, head), each block normalised
 by its own largest reference value."""
 import math
 
@@ -86,6 +86,35 @@ def test_many_short_sequences(io, C, D):
     assert rel_err(got[live], o_ref[live]) <= tol_for(io, torch.float32)
     assert np.all(got[~live] == 0)                                  # padding rows: zero output
     assert rel_err(np64(pool), p_ref) <= tol_for(io, torch.float32)
+
+
+@pytest.mark.parametrize("io", [torch.bfloat16, torch.float32])
+def test_repeated_calls_are_bitwise_identical(io):
+    """The kernels have no data-dependent reduction order, so repeated calls on the same inputs must
+    agree bit for bit: outputs, final states and every workspace record.  A race between threads
+    (a tile rewritten while another warp still reads it) shows up here as a difference between
+    calls, often in record parts that feed only the state."""
+    H, D = 8, 128
+    inp = workloads.make_inputs([1500, 64, 3, 700, 129, 1, 2048], H, D, io, pool_slots=8, pool_std=0.05,
+                                seed=1234, dt_bias_std=0.3)
+    d = workloads.to_device(inp, DEV)
+    params = kda.make_params(H, D, io_dtype=io, out_dtype=torch.float32, chunk_size=64)
+    n, T = d["state_idx"].numel(), d["q"].shape[0]
+    ws = torch.zeros(kda.prefill_workspace_size(params, n, T), dtype=torch.uint8, device=DEV)
+    first = None
+    for _ in range(8):
+        pool = d["pool"].clone()
+        out = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g_raw"], d["b_raw"], d["A_log"], d["dt_bias"],
+                                d["cu_seqlens"], pool, d["state_idx"], params=params, workspace=ws)
+        torch.cuda.synchronize()
+        assert kda.check_device_errors() == 0
+        got = (out.clone(), pool, ws.clone())
+        if first is None:
+            first = got
+            continue
+        assert torch.equal(got[0], first[0]), "outputs differ between calls"
+        assert torch.equal(got[1], first[1]), "states differ between calls"
+        assert torch.equal(got[2], first[2]), "workspace records differ between calls"
 
 
 def test_padding_rows_and_untouched_slots():
