@@ -6,21 +6,23 @@ One step = one pass of the whole path over one batch of synthetic input:
     bf16 q/k/v, fp32 gates, chunk 64, states from a 512-slot fp32 pool)       -> headline value
   * single-token decode (256 requests, H = 32, d = 128, pool updated in place) -> "decode"
   * scalar-gate verify (64 requests x 4 drafts, intermediate states written)  -> "verify"
-Every input lives in HBM before the timed region; each of the three working sets is larger than
-the 129 MB L2, so no L2 flush is needed between steps.  Kernel durations come from CUDA events
-recorded on the launching stream (the prefill's three kernels through kda_chunk_prefill_timed).
+  * buffered (ReplaySSM) decode of the decode workload, ring lengths 8 and 16
+                                                    -> "decode_replay", "decode_replay_l16"
+Every input lives in HBM before the timed region; each working set is larger than the 129 MB
+L2, so no L2 flush is needed between steps.  Kernel durations come from CUDA events recorded on
+the launching stream (the prefill's three kernels through kda_chunk_prefill_timed).
 
-  * buffered (ReplaySSM) decode of the decode workload                       -> "decode_replay"
 Outside the timed steps, on rank 0: the tiny fp32 prefill's launch latency ("tiny", us per call)
 and the long prefill, 1 sequence of 131072 tokens as 32 successive 4096-token calls carrying
 the state ("long_prefill").
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--only prefill]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--only prefill|decode]
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle instead, over the
 whole varlen workload per step, and prints the same metric.  ``--only prefill`` runs the varlen
-prefill alone (no decode, verify, tiny or long workloads, no e2e or CPU baseline): a small
-process for profiler captures.
+prefill alone (no decode, verify, tiny or long workloads, no e2e or CPU baseline) and ``--only
+decode`` the decode, verify and buffered-decode kernels alone: small processes for profiler
+captures, whose JSON line is not the bench line.
 """
 from __future__ import annotations
 
@@ -44,11 +46,11 @@ UNIT = "tokens/s"
 # step, caches flushed before each kernel), valid only for the kernel source they were taken on:
 # the hash covers the kernel's file and the two headers every kernel file includes.
 MEASURED_TRAFFIC = {
-    "kda_prefill.cu": {"sha256_16": "70923e2c089a3ec5",
-                       "kda_chunk_table": 0.02e6, "kda_chunk_intra": 1257.7e6, "kda_chunk_state": 761.1e6},
-    "kda_recurrent.cu": {"sha256_16": "55b03304299d9b86",
+    "kda_prefill.cu": {"sha256_16": "d09123f4b6f20b50",
+                       "kda_chunk_table": 0.02e6, "kda_chunk_intra": 1257.3e6, "kda_chunk_state": 766.4e6},
+    "kda_recurrent.cu": {"sha256_16": "3721675dd83df9a7",
                          "kda_recurrent_decode": 1022.1e6, "kda_recurrent_verify": 614.3e6,
-                         "kda_replay_decode_l8": 623.5e6, "kda_replay_decode_l16": 662.6e6},
+                         "kda_replay_decode_l8": 623.4e6, "kda_replay_decode_l16": 662.5e6},
 }
 TRAFFIC_HEADERS = ("kda_internal.cuh", "kda_tc.cuh")
 
