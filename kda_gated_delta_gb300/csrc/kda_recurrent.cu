@@ -67,19 +67,29 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src)
                  : "memory");
 }
 
-template <int D>
+// SPLIT CTAs share one (request, head), each owning D / SPLIT consecutive value rows of the state.
+template <int D, int SPLIT = 1>
 struct RecShape {
-    static constexpr int NWARPS = D >= 32 ? D / 16 : 1;
+    static constexpr int ROWS = D / SPLIT;          // state rows of one CTA
+    static constexpr int NWARPS = D >= 32 ? D / 16 / SPLIT : 1;
     static constexpr int THREADS = NWARPS * 32;
     static constexpr int CPL = D >= 32 ? 16 : 8;   // columns per lane
     static constexpr int LPR = D / CPL;             // lanes per row
     static constexpr int RPS = 32 / LPR;            // rows per warp step
-    static constexpr int ROWS_PER_WARP = D / NWARPS;
+    static constexpr int ROWS_PER_WARP = ROWS / NWARPS;
     static constexpr int STEPS = ROWS_PER_WARP / RPS;
     static constexpr int NV4 = CPL / 4;             // float4 groups per lane and row
     static_assert(ROWS_PER_WARP % RPS == 0, "row split");
-    static_assert(NWARPS * ROWS_PER_WARP == D, "rows");
+    static_assert(NWARPS * ROWS_PER_WARP == ROWS, "rows");
+    static_assert(THREADS >= D || SPLIT == 1, "one thread per channel in the prologue");
 };
+
+// The buffered decode at d = 128 runs two CTAs of 128 threads per (request, head), 64 state rows
+// each: a CTA streams its 32 KB of the checkpoint, and four CTAs fit on an SM instead of two, so
+// that more of the checkpoint is in flight while other CTAs work through the ring.  Both halves
+// form the per-channel prologue (norms, gate, ring products); rows are independent after it.
+template <int D, int MODE>
+__host__ __device__ constexpr int rec_split() { return MODE == kModeReplay && D == 128 ? 2 : 1; }
 
 // GATE: KDA_GATE_PER_CHANNEL or KDA_GATE_PER_HEAD.  MODE: kModeDecode updates the pool slot in
 // place; kModeVerify writes every intermediate state to `inter` and leaves the pool untouched;
@@ -87,10 +97,11 @@ struct RecShape {
 // the committed entries without materializing the state (readout decomposition), or (flush)
 // rebuilds the state from the checkpoint and ring and writes the new state to the checkpoint.
 template <int D, int GATE, int MODE, typename TIn, typename TOut>
-__global__ void __launch_bounds__(RecShape<D>::THREADS, (D >= 128 ? 2 : 4))
+__global__ void __launch_bounds__(RecShape<D, rec_split<D, MODE>()>::THREADS, (D >= 128 ? 2 * rec_split<D, MODE>() : 4))
 recurrent_kernel(const RecArgs a)
 {
-    using Sh = RecShape<D>;
+    constexpr int SPLIT = rec_split<D, MODE>();
+    using Sh = RecShape<D, SPLIT>;
     constexpr int NWARPS = Sh::NWARPS, CPL = Sh::CPL, LPR = Sh::LPR, RPS = Sh::RPS;
     constexpr int STEPS = Sh::STEPS, NV4 = Sh::NV4;
 
@@ -98,7 +109,9 @@ recurrent_kernel(const RecArgs a)
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int H = a.H;
-    const int64_t bh = blockIdx.x;
+    const int64_t bh = blockIdx.x / SPLIT;
+    const int half = SPLIT == 1 ? 0 : (int)(blockIdx.x % SPLIT);
+    const int row0 = half * Sh::ROWS;                // this CTA's first state row
     const int64_t b = bh / H;
     const int h = (int)(bh - b * H);
     constexpr bool VERIFY = MODE == kModeVerify;
@@ -123,7 +136,7 @@ recurrent_kernel(const RecArgs a)
     if (slot < 0) {  // padding row: zero outputs, no state traffic
         for (int t = 0; t < T; ++t) {
             const int64_t tok = b * T + t;
-            for (int j = tid; j < D; j += Sh::THREADS) out[(tok * H + h) * D + j] = from_f32<TOut>(0.f);
+            for (int j = row0 + tid; j < row0 + Sh::ROWS; j += Sh::THREADS) out[(tok * H + h) * D + j] = from_f32<TOut>(0.f);
         }
         return;
     }
@@ -187,7 +200,7 @@ recurrent_kernel(const RecArgs a)
     float4 st[STEPS][NV4];
 #pragma unroll
     for (int s = 0; s < STEPS; ++s) {
-        const int row = warp * Sh::ROWS_PER_WARP + s * RPS + row_in_step;
+        const int row = row0 + warp * Sh::ROWS_PER_WARP + s * RPS + row_in_step;
         const float4* src = reinterpret_cast<const float4*>(a.pool_in + tile + (size_t)row * D);
 #pragma unroll
         for (int j = 0; j < NV4; ++j) st[s][j] = __ldcs(src + li + LPR * j);
@@ -336,7 +349,7 @@ recurrent_kernel(const RecArgs a)
 #pragma unroll
             for (int j4 = 0; j4 < NV4; ++j4) kw[j4] = *reinterpret_cast<const float4*>(&s_rk[j * D + 4 * (li + LPR * j4)]);
 #pragma unroll
-            for (int s = 0; s < STEPS; ++s) dj[s] = s_rd[j * D + warp * Sh::ROWS_PER_WARP + s * RPS + row_in_step];
+            for (int s = 0; s < STEPS; ++s) dj[s] = s_rd[j * D + row0 + warp * Sh::ROWS_PER_WARP + s * RPS + row_in_step];
 #pragma unroll
             for (int s = 0; s < STEPS; ++s)
 #pragma unroll
@@ -401,7 +414,7 @@ recurrent_kernel(const RecArgs a)
         // ---- rows: decay, predict, error, write, read -----------------------------------------
 #pragma unroll
         for (int s = 0; s < STEPS; ++s) {
-            const int row = warp * Sh::ROWS_PER_WARP + s * RPS + row_in_step;
+            const int row = row0 + warp * Sh::ROWS_PER_WARP + s * RPS + row_in_step;
             const float vj = s_v[t * D + row];
             float pk = 0.f, pq = 0.f;
 #pragma unroll
@@ -454,7 +467,7 @@ recurrent_kernel(const RecArgs a)
 #pragma unroll
             for (int j = 0; j < NV4; ++j) __stcs(d4 + li + LPR * j, st[s][j]);
         }
-        if (MODE == kModeReplay && !flush) {          // append k_hat and the decay of this step
+        if (MODE == kModeReplay && !flush && half == 0) {   // append k_hat and the decay of this step
             const size_t re = ((size_t)slot * H + h) * a.ring_len + wp;
             for (int c = tid; c < D; c += Sh::THREADS) {
                 a.ring_k[re * D + c] = s_k[c] * rk1;
@@ -475,7 +488,8 @@ inline size_t recurrent_smem_bytes(int D, int T, int L)
 template <int D, int GATE, int MODE, typename TIn, typename TOut>
 cudaError_t launch_t(const RecArgs& a, int64_t batch, cudaStream_t stream)
 {
-    const int64_t blocks = batch * a.H;
+    constexpr int SPLIT = rec_split<D, MODE>();
+    const int64_t blocks = batch * a.H * SPLIT;
     if (blocks <= 0) return cudaSuccess;
     const size_t smem = recurrent_smem_bytes(D, MODE == kModeVerify ? a.t_draft : 1, MODE == kModeReplay ? a.ring_len : 0);
     if (smem > 48 * 1024) {
@@ -483,7 +497,7 @@ cudaError_t launch_t(const RecArgs& a, int64_t batch, cudaStream_t stream)
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    recurrent_kernel<D, GATE, MODE, TIn, TOut><<<(unsigned)blocks, RecShape<D>::THREADS, smem, stream>>>(a);
+    recurrent_kernel<D, GATE, MODE, TIn, TOut><<<(unsigned)blocks, RecShape<D, SPLIT>::THREADS, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
