@@ -117,6 +117,62 @@ def test_repeated_calls_are_bitwise_identical(io):
         assert torch.equal(got[2], first[2]), "workspace records differ between calls"
 
 
+def test_few_heads_long_sequences():
+    """Four heads and long sequences (up to 79 chunks), one padding and one empty sequence: outputs
+    and states match the oracle per (sequence, head), padding rows are zero, and a second call is
+    bitwise identical."""
+    H, D = 4, 128
+    inp = workloads.make_inputs([5000, 0, 3000, 4500], H, D, torch.bfloat16, pool_slots=6, pool_std=0.05,
+                                seed=4242, dt_bias_std=0.3, padding_rows=(2,))
+    d = workloads.to_device(inp, DEV)
+    params = kda.make_params(H, D, io_dtype=torch.bfloat16, out_dtype=torch.float32, chunk_size=64)
+    ws = torch.empty(kda.prefill_workspace_size(params, 4, d["q"].shape[0]), dtype=torch.uint8, device=DEV)
+    runs = []
+    for _ in range(2):
+        pool = d["pool"].clone()
+        out = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g_raw"], d["b_raw"], d["A_log"], d["dt_bias"],
+                                d["cu_seqlens"], pool, d["state_idx"], params=params, workspace=ws)
+        torch.cuda.synchronize()
+        assert kda.check_device_errors() == 0
+        runs.append((out, pool))
+    assert torch.equal(runs[0][0], runs[1][0]) and torch.equal(runs[0][1], runs[1][1])
+    o_ref, p_ref, _ = oracle_run(inp, H, D)
+    out, pool = runs[0]
+    cu = inp["cu_seqlens"]
+    assert rel_err(np64(out), o_ref) <= tol_for(torch.bfloat16, torch.float32)
+    assert rel_err(np64(pool), p_ref) <= tol_for(torch.bfloat16, torch.float32)
+    assert per_head_err(np64(out), o_ref, cu) <= PER_HEAD_BF16
+    assert per_head_err(np64(pool), p_ref) <= PER_HEAD_BF16
+    pad = slice(int(cu[2]), int(cu[3]))
+    assert bool((out[pad] == 0).all())                                # the padding sequence
+
+
+def test_prefill_under_graph_capture():
+    """A tensor-core prefill call captured in a CUDA graph and replayed gives the eager call's
+    outputs and states bit for bit (the entry point only enqueues work on the given stream)."""
+    H, D, T = 32, 128, 4096
+    inp = workloads.make_inputs([T], H, D, torch.bfloat16, pool_slots=1, pool_std=0.05, seed=77)
+    d = workloads.to_device(inp, DEV)
+    params = kda.make_params(H, D, io_dtype=torch.bfloat16, out_dtype=torch.bfloat16, chunk_size=64)
+    ws = torch.empty(kda.prefill_workspace_size(params, 1, T), dtype=torch.uint8, device=DEV)
+    pool_e = d["pool"].clone()
+    out_e = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g_raw"], d["b_raw"], d["A_log"], d["dt_bias"],
+                              d["cu_seqlens"], pool_e, d["state_idx"], params=params, workspace=ws)
+    torch.cuda.synchronize()
+    pool_g = d["pool"].clone()
+    out_g = torch.empty_like(out_e)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        kda.chunk_prefill(d["q"], d["k"], d["v"], d["g_raw"], d["b_raw"], d["A_log"], d["dt_bias"],
+                          d["cu_seqlens"], pool_g, d["state_idx"], out_g, params=params, workspace=ws)
+    pool_g.copy_(d["pool"])
+    g.replay()
+    torch.cuda.synchronize()
+    assert kda.check_device_errors() == 0
+    assert torch.equal(out_g, out_e)
+    assert torch.equal(pool_g, pool_e)
+
+
 def test_padding_rows_and_untouched_slots():
     H, D = 2, 64
     inp = workloads.make_inputs([20, 70, 3], H, D, torch.float32, pool_slots=6, pool_std=0.1, seed=3,
