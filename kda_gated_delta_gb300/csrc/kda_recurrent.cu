@@ -22,7 +22,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "kda_internal.cuh"
+#include "kda_tc.cuh"
 
 namespace kda {
 namespace {
@@ -55,6 +58,7 @@ struct RecArgs {
     int ring_len;             // L
     const int32_t* write_pos; // [batch] entries committed in the ring (0 .. L-1)
     const int32_t* force_flush;  // [batch] or null
+    int64_t prefetch_ahead;   // CTAs between this one and the one whose state it prefetches into L2; 0 off
 };
 
 enum { kModeDecode = 0, kModeVerify = 1, kModeReplay = 2 };
@@ -204,6 +208,20 @@ recurrent_kernel(const RecArgs a)
         const float4* src = reinterpret_cast<const float4*>(a.pool_in + tile + (size_t)row * D);
 #pragma unroll
         for (int j = 0; j < NV4; ++j) st[s][j] = __ldcs(src + li + LPR * j);
+    }
+    // L2 prefetch of the state rows of the CTA prefetch_ahead places later in the grid: CTAs start in
+    // index order, so that one starts about one CTA lifetime from now and finds its state in L2.
+    // Registers cap the state bytes the resident CTAs hold in flight; an L2 prefetch takes none.
+    if (tid == 0 && a.prefetch_ahead > 0) {
+        const int64_t nb = (int64_t)blockIdx.x + a.prefetch_ahead;
+        if (nb < (int64_t)gridDim.x) {
+            const int64_t bh2 = nb / SPLIT, b2 = bh2 / H;
+            const int h2 = (int)(bh2 - b2 * H);
+            const int64_t slot2 = a.state_idx[b2];
+            if (slot2 >= 0 && slot2 < a.num_slots)
+                tc::bulk_prefetch_l2(a.pool_in + ((size_t)slot2 * H + h2) * (size_t)D * D + (size_t)(nb % SPLIT) * Sh::ROWS * D,
+                                     (uint32_t)(Sh::ROWS * D * sizeof(float)));
+        }
     }
 
     const float rate = expf(a_log);
@@ -497,7 +515,30 @@ cudaError_t launch_t(const RecArgs& a, int64_t batch, cudaStream_t stream)
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    recurrent_kernel<D, GATE, MODE, TIn, TOut><<<(unsigned)blocks, RecShape<D, SPLIT>::THREADS, smem, stream>>>(a);
+    // resident CTAs on the device (computed once per device and shared memory size class): the
+    // prefetch distance; no prefetch if the occupancy query fails
+    static std::atomic<int> resident[64][2];
+    const int cls = smem > 48 * 1024 ? 1 : 0;
+    int dev = 0;
+    RecArgs la = a;
+    la.prefetch_ahead = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
+        int r = resident[dev][cls].load(std::memory_order_relaxed);
+        if (r == 0) {
+            int per_sm = 0, sms = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, recurrent_kernel<D, GATE, MODE, TIn, TOut>,
+                                                              RecShape<D, SPLIT>::THREADS, smem) == cudaSuccess &&
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && per_sm * sms > 0) {
+                r = per_sm * sms;
+            } else {
+                cudaGetLastError();
+                r = -1;
+            }
+            resident[dev][cls].store(r, std::memory_order_relaxed);
+        }
+        if (r > 0) la.prefetch_ahead = r;
+    }
+    recurrent_kernel<D, GATE, MODE, TIn, TOut><<<(unsigned)blocks, RecShape<D, SPLIT>::THREADS, smem, stream>>>(la);
     return cudaGetLastError();
 }
 
