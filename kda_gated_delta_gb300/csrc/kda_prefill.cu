@@ -1151,10 +1151,6 @@ namespace itc {
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 __device__ __forceinline__ float4 mul4(float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); }
-__device__ __forceinline__ float4 rnd4(float4 a)
-{
-    return make_float4(tc::round_tf32(a.x), tc::round_tf32(a.y), tc::round_tf32(a.z), tc::round_tf32(a.w));
-}
 __device__ __forceinline__ float ex2_approx(float x)
 {
     float y;
@@ -1253,18 +1249,17 @@ constexpr uint32_t OFF_BAR = OFF_BETA + C * 4;       // 4 mbarriers: Gram done, 
 constexpr uint32_t OFF_TM = OFF_BAR + 32;            // TMEM base
 constexpr uint32_t BYTES = OFF_TM + 16;
 constexpr uint32_t OFF_A = OFF_K;                    // A = sum of diagonal and Gram blocks [C][LDA]
-constexpr uint32_t OFF_X = OFF_K + C * LDA * 4;      // 3 scratch 16 x 16 blocks
 constexpr uint32_t OFF_IB = OFF_Q;                   // Gram B image: 96 rows x 128 fp16
-constexpr uint32_t OFF_T = OFF_AL;                   // T [C][LDA]
-constexpr uint32_t OFF_IT = OFF_AL + C * LDA * 4;    // T image (rows r, K = j), tf32
-static_assert(OFF_X + 3 * 256 * 4 <= OFF_Q, "A and X fit in the k tile");
+constexpr uint32_t OFF_T = OFF_AL;                   // diagonal blocks T_II of (I + A)^{-1} [C][LDA]
+constexpr uint32_t OFF_IT = OFF_AL + C * LDA * 4;    // 10 tf32 16 x 16 images: T_II and -F_IJ
+static_assert(OFF_A + C * LDA * 4 <= OFF_Q, "A fits in the k tile");
 static_assert(96 * D * 2 <= TILE, "the fp16 B image fits in the q tile");
-static_assert(OFF_IT + C * C * 4 <= OFF_AD, "T and its image fit in the alpha tile");
+static_assert(OFF_IT + 10 * 256 * 4 <= OFF_AD, "T_II and the block images fit in the alpha tile");
 static_assert(2 * (BYTES + 1024) <= 233472, "two CTAs per SM");
 // TMEM columns (256 allocated)
 constexpr uint32_t T_KD = 0;      // decayed keys, fp16 pairs (64 cols); then (beta V)^T (64)
 constexpr uint32_t T_KB = 64;     // (beta Kbar)^T (64)
-constexpr uint32_t T_G = 128;     // Gram result (96); then U^T (64) and W^T (64)
+constexpr uint32_t T_G = 128;     // Gram result (96); then U^T (64) and W^T (64), built block by block
 }  // namespace itc
 
 // The chunk's k, q (bf16) and g (fp32) tiles arrive by tensor-map copies (cp.async.bulk.tensor) issued
@@ -1285,7 +1280,6 @@ chunk_intra_tc_kernel(const IntraArgs a, const __grid_constant__ CUtensorMap tm_
     float* sB12 = reinterpret_cast<float*>(sm + OFF_B12);
     float* sBeta = reinterpret_cast<float*>(sm + OFF_BETA);
     float* sA = reinterpret_cast<float*>(sm + OFF_A);
-    float* sX = reinterpret_cast<float*>(sm + OFF_X);
     float* sT = reinterpret_cast<float*>(sm + OFF_T);
     float* sIT = reinterpret_cast<float*>(sm + OFF_IT);
     unsigned char* sIB = sm + OFF_IB;
@@ -1694,7 +1688,15 @@ chunk_intra_tc_kernel(const IntraArgs a, const __grid_constant__ CUtensorMap tm_
     tc::tc_fence_before();
     __syncthreads();
 
-    // 6. T = (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution, then by block distance
+    // 6. U = (I + A)^{-1} diag(beta) V and W = (I + A)^{-1} diag(beta) Kbar by block forward
+    //    substitution over the four 16-row blocks: X_I = T_II B_I - sum_{J<I} F_IJ X_J with
+    //    T_II = (I + A_II)^{-1}, F_IJ = T_II A_IJ and B = [beta V | beta Kbar].  The diagonal inverses
+    //    (one column per thread) and the six F_IJ are formed on CUDA cores; every product with the
+    //    128 value and key channels runs on the tensor core in the transposed form
+    //    X_I^T = B_I^T T_II^T - sum_J X_J^T F_IJ^T (lane = channel, N = 16 rows of block I): all four
+    //    B_I^T T_II^T first, then three rounds in which the block just completed is rounded to tf32
+    //    into the operand columns its B_J^T no longer needs and every remaining product with it is
+    //    issued.
     if (tid < C) {
         const int I = tid >> 4, jj = tid & 15, j = tid;
         float col[16];
@@ -1711,68 +1713,78 @@ chunk_intra_tc_kernel(const IntraArgs a, const __grid_constant__ CUtensorMap tm_
         for (int i = 0; i < 16; ++i) sT[(16 * I + i) * LDA + j] = col[i];
     }
     __syncthreads();
-    auto tblocks = [&](auto dc) {
-        constexpr int d = decltype(dc)::value;
-        constexpr int nb = NB - d;
-        for (int e = tid; e < nb * 256; e += THREADS) {      // X_IJ = sum_{J<=K<I} A_IK T_KJ
-            const int J = e >> 8, I = J + d, i = (e >> 4) & 15, jj = e & 15;
-            const float* ar = sA + (16 * I + i) * LDA + 16 * J;
-            const float* tc0 = sT + 16 * J * LDA + 16 * J + jj;
+    // tf32 images (rows r, K = j; 16 x 16, 1 KB, cores [r/8][j/4][r%8][j%4]): slots 0..3 T_II, slots
+    // 4..9 -F_IJ for (I, J) = (1,0) (2,0) (3,0) (2,1) (3,1) (3,2)
+    for (int e = tid; e < 10 * 256; e += THREADS) {
+        const int slot = e >> 8, r = (e >> 4) & 15, j = e & 15;
+        float x;
+        if (slot < 4) {
+            x = sT[(16 * slot + r) * LDA + 16 * slot + j];
+        } else {
+            const int f = slot - 4;
+            const int I = f < 3 ? f + 1 : (f < 5 ? f - 1 : 3), J = f < 3 ? 0 : (f < 5 ? 1 : 2);
+            const float* tr = sT + (16 * I + r) * LDA + 16 * I;        // T_II is unit lower triangular
+            const float* ac = sA + (16 * I) * LDA + 16 * J + j;
             float acc = 0.f;
 #pragma unroll
-            for (int kk = 0; kk < 16 * d; kk += 4) {                // a row of A as float4s
-                const float4 av = ld4(ar + kk);
-                acc = fmaf(av.x, tc0[kk * LDA], acc);
-                acc = fmaf(av.y, tc0[(kk + 1) * LDA], acc);
-                acc = fmaf(av.z, tc0[(kk + 2) * LDA], acc);
-                acc = fmaf(av.w, tc0[(kk + 3) * LDA], acc);
+            for (int k = 0; k < 16; k += 4) {
+                const float4 tv = ld4(tr + k);
+                acc = k + 0 <= r ? fmaf(tv.x, ac[(k + 0) * LDA], acc) : acc;
+                acc = k + 1 <= r ? fmaf(tv.y, ac[(k + 1) * LDA], acc) : acc;
+                acc = k + 2 <= r ? fmaf(tv.z, ac[(k + 2) * LDA], acc) : acc;
+                acc = k + 3 <= r ? fmaf(tv.w, ac[(k + 3) * LDA], acc) : acc;
             }
-            sX[e] = acc;
+            x = -acc;
         }
-        __syncthreads();
-        for (int e = tid; e < nb * 256; e += THREADS) {      // T_IJ = -T_II X_IJ
-            const int J = e >> 8, I = J + d, i = (e >> 4) & 15, jj = e & 15;
-            const float* tr = sT + (16 * I + i) * LDA + 16 * I;
-            const float* xc = sX + (J << 8) + jj;
-            float acc = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < 16; kk += 4) {                    // T_II is lower triangular
-                const float4 tv = ld4(tr + kk);
-                acc = kk + 0 <= i ? fmaf(tv.x, xc[kk * 16], acc) : acc;
-                acc = kk + 1 <= i ? fmaf(tv.y, xc[(kk + 1) * 16], acc) : acc;
-                acc = kk + 2 <= i ? fmaf(tv.z, xc[(kk + 2) * 16], acc) : acc;
-                acc = kk + 3 <= i ? fmaf(tv.w, xc[(kk + 3) * 16], acc) : acc;
-            }
-            sT[(16 * I + i) * LDA + 16 * J + jj] = -acc;
-        }
-        __syncthreads();
-    };
-    tblocks(std::integral_constant<int, 1>{});
-    tblocks(std::integral_constant<int, 2>{});
-    tblocks(std::integral_constant<int, 3>{});
-
-    // T image (rows r, K = j); U^T = (beta V)^T T^T, W^T = (beta Kbar)^T T^T
-    for (int f = tid; f < C * C / 4; f += THREADS) {
-        const int core = f >> 3, rr = (core >> 4) * 8 + (f & 7), j0 = (core & 15) * 4;
-        st4(sIT + 4 * f, rnd4(ld4(sT + rr * LDA + j0)));
+        sIT[slot * 256 + (((r >> 3) * 4 + (j >> 2)) << 5) + ((r & 7) << 2) + (j & 3)] = tc::round_tf32(x);
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc::tc_fence_before();
     __syncthreads();
+    const uint32_t bImg = tc::smem_u32(sIT);
+    // (I, J) block product into both halves: J < 0 is B_I^T T_II^T (accumulator cleared), else
+    // X_J^T (-F_IJ)^T added; A from TMEM (tf32), B the 1 KB image, K = 16 in two steps of 8
+    auto uw_mma = [&](int I, int J, int slot) {
+        constexpr uint32_t idesc = tc::idesc_tf32(128, 16);
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int s2 = 0; s2 < 2; ++s2)
+                tc::mma_tf32_ts(tmem + T_G + 64 * part + 16 * I, tmem + (part ? T_KB : T_KD) + 16 * (J < 0 ? I : J) + 8 * s2,
+                                tc::smem_desc(bImg + 1024 * slot + 256 * s2, 128, 512), idesc, J >= 0 || s2 > 0);
+    };
     if (tid == 0) {
         tc::tc_fence_after();
-        constexpr uint32_t idesc = tc::idesc_tf32(128, 64);
-        const uint32_t bT = tc::smem_u32(sIT);
-#pragma unroll
-        for (int s = 0; s < C / 8; ++s)
-            tc::mma_tf32_ts(tmem + T_G, tmem + T_KD + 8 * s, tc::smem_desc(bT + 256 * s, 128, 2048), idesc, s > 0);
-#pragma unroll
-        for (int s = 0; s < C / 8; ++s)
-            tc::mma_tf32_ts(tmem + T_G + 64, tmem + T_KB + 8 * s, tc::smem_desc(bT + 256 * s, 128, 2048), idesc, s > 0);
+        for (int I = 0; I < NB; ++I) uw_mma(I, -1, I);
         tc::mma_commit(bar_uw);
     }
+    bool done = true;
+    const int hf_uw = warp >> 2;                  // warps 0..3: the U half, 4..7: the W half
+#pragma unroll 1
+    for (int J = 0; J < NB - 1; ++J) {
+        // block J is complete (round J); round it to tf32 into the columns of B_J^T
+        const bool ok = tc::mbar_wait(bar_uw, J & 1, kWaitPolls);
+        done = done && ok;
+        tc::tc_fence_after();
+        if (ok) {
+            float x[16];
+            tc::tmem_ld16(tmem + lane_base + T_G + 64 * hf_uw + 16 * J, x);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[i] = tc::round_tf32(x[i]);
+            tc::tmem_st16_nowait(tmem + lane_base + (hf_uw ? T_KB : T_KD) + 16 * J, x);
+            tc::tmem_wait_st();
+        }
+        tc::tc_fence_before();
+        __syncthreads();
+        if (tid == 0 && done) {
+            tc::tc_fence_after();
+            // every product with X_J: (I, J) for I > J; slots of -F_IJ in the order above
+            for (int I = J + 1; I < NB; ++I) uw_mma(I, J, 4 + (J == 0 ? I - 1 : (J == 1 ? I + 1 : 5)));
+            tc::mma_commit(bar_uw);
+        }
+    }
     {
-        const bool done = tc::mbar_wait(bar_uw, 0, kWaitPolls);
+        done = tc::mbar_wait(bar_uw, (NB - 1) & 1, kWaitPolls) && done;   // round NB - 1: block 3 complete
         tc::tc_fence_after();
         if (tid == 0) tc_ok = tc_ok && done;
         if (!done) {
