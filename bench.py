@@ -46,11 +46,11 @@ UNIT = "tokens/s"
 # step, caches flushed before each kernel), valid only for the kernel source they were taken on:
 # the hash covers the kernel's file and the two headers every kernel file includes.
 MEASURED_TRAFFIC = {
-    "kda_prefill.cu": {"sha256_16": "d09123f4b6f20b50",
-                       "kda_chunk_table": 0.02e6, "kda_chunk_intra": 1256.8e6, "kda_chunk_state": 767.0e6},
-    "kda_recurrent.cu": {"sha256_16": "e2125596fb8e3c85",
-                         "kda_recurrent_decode": 1022.5e6, "kda_recurrent_verify": 614.3e6,
-                         "kda_replay_decode_l8": 625.6e6, "kda_replay_decode_l16": 665.2e6},
+    "kda_prefill.cu": {"sha256_16": "b2c9567edaece85f",
+                       "kda_chunk_table": 0.02e6, "kda_chunk_intra": 1257.6e6, "kda_chunk_state": 766.1e6},
+    "kda_recurrent.cu": {"sha256_16": "b92d5644c888e5ec",
+                         "kda_recurrent_decode": 1022.4e6, "kda_recurrent_verify": 617.3e6,
+                         "kda_replay_decode_l8": 643.1e6, "kda_replay_decode_l16": 674.0e6},
 }
 TRAFFIC_HEADERS = ("kda_internal.cuh", "kda_tc.cuh")
 
