@@ -1762,8 +1762,9 @@ chunk_intra_tc_kernel(const IntraArgs a, const __grid_constant__ CUtensorMap tm_
     const int hf_uw = warp >> 2;                  // warps 0..3: the U half, 4..7: the W half
 #pragma unroll 1
     for (int J = 0; J < NB - 1; ++J) {
-        // block J is complete (round J); round it to tf32 into the columns of B_J^T
-        const bool ok = tc::mbar_wait(bar_uw, J & 1, kWaitPolls);
+        // block J is complete (round J); round it to tf32 into the columns of B_J^T (the TMEM
+        // accesses below are warp-collective: the warp goes on only if all its lanes saw the phase)
+        const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_uw, J & 1, kWaitPolls));
         done = done && ok;
         tc::tc_fence_after();
         if (ok) {
@@ -1784,7 +1785,7 @@ chunk_intra_tc_kernel(const IntraArgs a, const __grid_constant__ CUtensorMap tm_
         }
     }
     {
-        done = tc::mbar_wait(bar_uw, (NB - 1) & 1, kWaitPolls) && done;   // round NB - 1: block 3 complete
+        done = __all_sync(0xffffffffu, tc::mbar_wait(bar_uw, (NB - 1) & 1, kWaitPolls) && done);   // block 3 complete
         tc::tc_fence_after();
         if (tid == 0) tc_ok = tc_ok && done;
         if (!done) {
