@@ -46,7 +46,7 @@ UNIT = "tokens/s"
 # step, caches flushed before each kernel), valid only for the kernel source they were taken on:
 # the hash covers the kernel's file and the two headers every kernel file includes.
 MEASURED_TRAFFIC = {
-    "kda_prefill.cu": {"sha256_16": "51cdf50bb9dc361b",
+    "kda_prefill.cu": {"sha256_16": "fa729363c4e70a4f",
                        "kda_chunk_table": 0.02e6, "kda_chunk_intra": 1257.3e6, "kda_chunk_state": 766.4e6},
     "kda_recurrent.cu": {"sha256_16": "b92d5644c888e5ec",
                          "kda_recurrent_decode": 1022.3e6, "kda_recurrent_verify": 616.9e6,

@@ -1216,11 +1216,12 @@ __device__ __forceinline__ void gram_row(int m, int& I, int& j)
 }  // namespace itc
 
 // ---- intra-chunk kernel for bf16 inputs at C = 64, D = 128: two CTAs per SM -----------------------
-// One CTA of 256 threads per (chunk, head) with 105 KB of shared memory and 256 TMEM columns, so
+// One CTA of 256 threads per (chunk, head) with 110 KB of shared memory and 256 TMEM columns, so
 // that two CTAs share an SM and each one's loads, barriers and single-thread MMA issue overlap the
 // other's arithmetic.  Three [C][LD] fp32 tiles hold k_hat, q_hat and alpha; each is reused in
 // place as the pass over it ends.  It writes the tensor-core record (HRec) that the state pass reads:
-//   1. loads; alpha = e^{g} (MUFU form of the gate); L2 norms fused into the loads
+//   1. k, q and g tiles by tensor-map TMA copies; alpha = e^{g} (MUFU form of the gate) and the L2
+//      norms applied as the staged tiles are rewritten
 //   2. diagonal 16 x 16 sub-blocks of A and P by running products of alphas (CUDA cores); each
 //      thread takes key rows j and 15 - j so that all warps do the same number of rows; P goes
 //      straight to the record image, A to a small buffer
@@ -1230,16 +1231,17 @@ __device__ __forceinline__ void gram_row(int m, int& I, int& j)
 //      magnitude): B image = rows of k o Rin and q o Rin of blocks 1..3 (over the q tile), A = key
 //      j decayed to the start of row block I in TMEM (lane m <-> (I, j)); Qbar record
 //   5. while the MMA runs: value loads for (beta V)^T; Gram result -> off-diagonal A and P
-//   6. T = (I + A)^{-1} by blocks (over the alpha tile), then U^T = (beta V)^T T^T and
-//      W^T = (beta Kbar)^T T^T with both A operands in TMEM (kind::tf32)
+//   6. U and W by block forward substitution: the diagonal inverses T_II and F_IJ = T_II A_IJ on
+//      CUDA cores (over the alpha tile), every product with the value and key channels as
+//      kind::tf32 MMAs with the A operands in TMEM
 namespace itc {
 constexpr int C = 64, D = 128, NB = 4, THREADS = 256;
 constexpr int LD = 132;   // padded row stride (floats) of the [C][D] tiles
 constexpr int LDA = 68;   // padded row stride of the [C][C] tiles
 constexpr uint32_t TILE = C * LD * 4;
-constexpr uint32_t OFF_K = 0;                        // k_hat -> k o Rin; then A and X
+constexpr uint32_t OFF_K = 0;                        // k_hat -> k o Rin; then A
 constexpr uint32_t OFF_Q = TILE;                     // q_hat -> q o Rin; then the Gram B image
-constexpr uint32_t OFF_AL = 2 * TILE;                // alpha -> k o Rout; then T and its image
+constexpr uint32_t OFF_AL = 2 * TILE;                // alpha -> k o Rout; then T_II and the block images
 constexpr uint32_t OFF_AD = 3 * TILE;                // diagonal blocks of A   [NB][16][16]
 constexpr uint32_t OFF_BP = OFF_AD + NB * 256 * 4;   // block products bp      [NB][D]
 constexpr uint32_t OFF_EB = OFF_BP + NB * D * 4;     // e^{G} before block b: prod_{b' < b} bp  [NB][D]
