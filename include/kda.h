@@ -33,8 +33,10 @@
  *     work is enqueued and return a status without touching memory.  Work is then enqueued on
  *     `stream` and the call returns without synchronising; a launch failure is reported as
  *     KDA_ERR_CUDA.  No call aborts, throws or prints.
- *   - The entry points keep no host state between calls and may be called from several host
- *     threads on different streams.  Calls on the same state slots must be ordered by the caller.
+ *   - The entry points keep no state between calls beyond device properties looked up once per
+ *     process (the driver's tensor-map encoder; the number of CTAs of each recurrent kernel that
+ *     fit on a device at once), and may be called from several host threads on different
+ *     streams.  Calls on the same state slots must be ordered by the caller.
  */
 #ifndef KDA_H
 #define KDA_H
