@@ -1,8 +1,8 @@
 """Pins of the fp64 oracle against what the pages and the mathematics fix, independently of the
 oracle's own formulas: the overwrite property, orthonormal readback, the prefix-sum special case,
 the gradient-step (online regression) identity, the beta-interpolation identity, contraction,
-the compact matrix form, GDN as a special case of KDA, the printed safe-gate example and the
-chunk closed form.  CPU only."""
+the compact matrix form, GDN as a special case of KDA, the printed safe-gate example, the
+explicit q scale, the argument checks and the chunk closed form.  CPU only."""
 import math
 import os
 
@@ -319,6 +319,48 @@ def test_verify_mode_intermediate_states():
             pool_step = torch.tensor(pnew)
             assert np.array_equal(o[0], out_v[row])
             assert np.array_equal(pnew[int(inp["state_idx"][b])], inter[row])
+
+
+def test_explicit_scale_multiplies_outputs_only():
+    """q enters the recurrence only through the read o_t = q_t S_t ("linear_attention", the
+    per-token reference: q is scaled after its normalisation, the state update never sees q).
+    An explicit scale s therefore multiplies every output by s / d_k^{-1/2} and leaves every
+    state exactly as the default scale does."""
+    import torch
+    H, D = 2, 8
+    inp = workloads.make_inputs([6, 9], H, D, torch.float32, pool_slots=3, pool_std=0.1, seed=31,
+                                dt_bias_std=0.5)
+    args = (inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["b_raw"], inp["A_log"], inp["dt_bias"],
+            inp["cu_seqlens"], inp["pool"], inp["state_idx"])
+    o_d, p_d, _ = oracle.forward(oracle.make_params(H, D), *args)
+    s = 0.7
+    for chunk in (None, 4):
+        o_s, p_s, _ = oracle.forward(oracle.make_params(H, D, scale=s), *args, chunk_size=chunk)
+        assert np.allclose(o_s, o_d * (s * math.sqrt(D)), rtol=1e-12, atol=1e-15)
+        if chunk is None:
+            assert np.array_equal(p_s, p_d)
+        else:
+            assert np.allclose(p_s, p_d, rtol=1e-12, atol=1e-15)
+
+
+def test_argument_checks():
+    """Host-side rejections of the oracle: a slot index equal to the pool's slot count and a
+    decreasing cu_seqlens are refused before any arithmetic; the last valid slot is accepted."""
+    import torch
+    H, D = 1, 4
+    inp = workloads.make_inputs([3, 2], H, D, torch.float32, pool_slots=2, seed=33)
+    p = oracle.make_params(H, D)
+
+    def call(**over):
+        a = dict(inp, **over)
+        return oracle.forward(p, a["q"], a["k"], a["v"], a["g_raw"], a["b_raw"], a["A_log"],
+                              a["dt_bias"], a["cu_seqlens"], a["pool"], a["state_idx"])
+
+    call(state_idx=torch.tensor([0, 1], dtype=torch.int32))
+    with pytest.raises(ValueError):
+        call(state_idx=torch.tensor([0, 2], dtype=torch.int32))
+    with pytest.raises(ValueError):
+        call(cu_seqlens=torch.tensor([0, 3, 2], dtype=torch.int32))
 
 
 # ---------------------------------------------------------------------------------------------
