@@ -13,7 +13,8 @@ random interleavings:
     commit arrives once all of its issuer's earlier MMAs have executed; copies land in any order;
   * every operand an MMA or a warp reads must hold the chunk's version the algorithm needs when it
     is read (no buffer reused too early);
-  * the run must finish (no deadlock).
+  * the run must finish (no deadlock), and the copy warp's closing drain must leave no copy in
+    flight when that warp exits.
 
 The model has to be kept in step with the kernel by hand: it mirrors the kernel's wait lists,
 buffer indices and arrival counts, not its arithmetic.
@@ -35,9 +36,15 @@ class Bar:
                 self.phase += 1
 
 
+def last_phase(n, s, depth):
+    """Phase of ring slot s after n copies: it last received chunk s + depth ((n - 1 - s) // depth)."""
+    return (n - 1 - s) // depth
+
+
 class Model:
-    def __init__(self, n, seed, single_delta_barrier=False):
+    def __init__(self, n, seed, single_delta_barrier=False, drain_phase=last_phase):
         self.n, self.rng = n, random.Random(seed)
+        self.drain_phase = drain_phase
         self.w = [Bar(f"w{i}") for i in range(4)]
         self.kt = [Bar(f"kt{i}") for i in range(3)]
         self.u = [Bar(f"u{i}") for i in range(2)]
@@ -166,6 +173,11 @@ def copy_warp(M):                     # warp 18
         if i + 2 < n:
             yield ring(M.o, i, 2)
             qp(i + 2)
+    # drain: the copies still in flight land before the CTA exits
+    for bars, depth in ((M.w, 4), (M.kt, 3), (M.u, 2), (M.qp, 2)):
+        for s in range(min(depth, n)):
+            ph = M.drain_phase(n, s, depth)
+            yield (bars[s], ph & 1, ph)
 
 
 def delta_pass(M):                    # warps 0..3
@@ -222,8 +234,8 @@ def z_w_output_warps(M):              # warps 12..15
         M.do_free.arrive(128)
 
 
-def run(n, seed, single_delta_barrier=False):
-    M = Model(n, seed, single_delta_barrier)
+def run(n, seed, single_delta_barrier=False, drain_phase=last_phase):
+    M = Model(n, seed, single_delta_barrier, drain_phase)
     roles = {"chain+(c)": chain_and_c_issuer(M), "Z+out": z_and_output_issuer(M), "copies": copy_warp(M),
              "Delta": delta_pass(M), "S": state_update(M), "Z/W'/out warps": z_w_output_warps(M)}
     waiting, done = {}, set()
@@ -233,6 +245,8 @@ def run(n, seed, single_delta_barrier=False):
             waiting[k] = next(roles[k])
         except StopIteration:
             done.add(k)
+            if k == "copies":
+                assert not M.copies, f"the copy warp exits with {len(M.copies)} copies in flight"
 
     for k in roles:
         step(k)
@@ -287,4 +301,18 @@ def test_single_delta_barrier_is_caught():
             run(5, seed, single_delta_barrier=True)
         except AssertionError:
             failures += 1
+    assert failures > 0
+
+
+@pytest.mark.parametrize("wrong", [lambda n, s, d: (n - s) // d, lambda n, s, d: (n - 1 - s) // d - 1])
+def test_wrong_drain_phase_is_caught(wrong):
+    """A drain that waits one phase too far never ends; one that waits one phase too early lets
+    the copy warp exit with its last copies in flight."""
+    failures = 0
+    for n in (1, 3, 5, 8):
+        for seed in range(10):
+            try:
+                run(n, seed, drain_phase=wrong)
+            except AssertionError:
+                failures += 1
     assert failures > 0
