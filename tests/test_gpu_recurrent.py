@@ -128,6 +128,36 @@ def test_verify_small(gate, D, io):
     assert np.all(np64(out)[4 * Td:5 * Td] == 0.0)
 
 
+@pytest.mark.parametrize("gate", ["kda", "gdn"])
+@pytest.mark.parametrize("Td", [1, 16])
+def test_verify_draft_count_bounds(gate, Td):
+    """t_draft at both ends of its range (1 and 16) at d = 128: outputs and every intermediate state
+    against the oracle, then the commit of the last draft's state against the oracle's state after
+    that draft."""
+    H, D, B = 4, 128, 5
+    inp = workloads.make_inputs([Td] * B, H, D, torch.bfloat16, gate=gate, pool_slots=7, pool_std=0.05,
+                                seed=91 + Td, dt_bias_std=0.3, padding_rows=(3,))
+    out, inter = run_verify(inp, Td, gate)
+    assert kda.check_device_errors() == 0
+    o_ref, _, i_ref = oracle_run(inp, H, D, gate=gate, inter=True)
+    tol = tol_for(torch.bfloat16, torch.float32)
+    assert rel_err(np64(out), o_ref) <= tol
+    inter_np = np64(inter).reshape(B * Td, H, D, D)
+    valid = [b for b in range(B) if b != 3]
+    rows = [b * Td + t for b in valid for t in range(Td)]
+    assert rel_err(inter_np[rows], i_ref[rows]) <= tol
+    assert np.all(np64(out)[3 * Td:4 * Td] == 0.0)
+    d = workloads.to_device(inp, DEV)
+    pool = d["pool"].clone()
+    accept = torch.full((B,), Td, dtype=torch.int32, device=DEV)
+    kda.commit_verified_states(inter, accept, pool, d["state_idx"], gate=gate)
+    torch.cuda.synchronize()
+    assert kda.check_device_errors() == 0
+    for b in valid:
+        s = int(inp["state_idx"][b])
+        assert rel_err(np64(pool[s]), i_ref[b * Td + Td - 1]) <= tol
+
+
 def test_verify_full_workload_gdn():
     """Scalar-gate verify: 64 requests x 4 drafts, H = 32, d = 128, all intermediate states."""
     inp = workloads.workload_inputs(4)
