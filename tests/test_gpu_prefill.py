@@ -57,6 +57,20 @@ def test_edge_shapes_bf16(lengths):
     check(inp, H, D, 64, torch.bfloat16)
 
 
+@pytest.mark.parametrize("H", [1, 7, 64])
+def test_tensor_core_pair_head_counts(H):
+    """The bf16, d = 128, chunk 64 pair with one head, an odd head count and 64 heads: the tensor
+    maps' row pitch (H x 128 elements) and the (chunk, head) indexing of the records."""
+    D = 128
+    inp = workloads.make_inputs([130, 64, 1], H, D, torch.bfloat16, pool_slots=4, pool_std=0.05, seed=500 + H,
+                                dt_bias_std=0.5)
+    out, pool, _, _ = check(inp, H, D, 64, torch.bfloat16)
+    o_ref, p_ref, _ = oracle_run(inp, H, D)
+    used = inp["state_idx"].long()
+    assert per_head_err(np64(out), o_ref, inp["cu_seqlens"].tolist()) <= PER_HEAD_BF16
+    assert per_head_err(np64(pool)[used], p_ref[used]) <= PER_HEAD_BF16
+
+
 @pytest.mark.parametrize("C,D", [(16, 16), (16, 32), (32, 64), (64, 64), (16, 128), (32, 128), (64, 32)])
 @pytest.mark.parametrize("io", [torch.float32, torch.bfloat16])
 def test_chunk_and_dim_grid(C, D, io):
