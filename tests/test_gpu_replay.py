@@ -38,6 +38,33 @@ def test_ring_length_one_is_plain_decode(gate, D):
         assert torch.equal(pool_a, pool_b)
 
 
+@pytest.mark.parametrize("H", [1, 7])
+def test_replay_odd_head_counts(H):
+    """d = 128 runs two CTAs per (request, head); with one head and with an odd head count each CTA
+    still finds its request, head and half of the rows."""
+    D, L, B, steps = 128, 8, 5, 12
+    inp = workloads.make_inputs([steps] * B, H, D, torch.bfloat16, pool_slots=6, pool_std=0.05, seed=600 + H,
+                                dt_bias_std=0.3)
+    o_ref, p_ref, _ = oracle_run(inp, H, D)
+    d = workloads.to_device(inp, DEV)
+    pool = d["pool"].clone()
+    rings = kda.replay_rings(6, H, D, L, device=DEV)
+    pos = np.zeros(B, dtype=np.int32)
+    tol = tol_for(torch.bfloat16, torch.float32)
+    for t in range(steps):
+        force = np.zeros(B, dtype=np.int32) if t < steps - 1 else np.ones(B, dtype=np.int32)
+        x = _step_rows(inp, B, steps, t)
+        o = kda.replay_decode(x["q"], x["k"], x["v"], x["g_raw"], x["b_raw"], d["A_log"], d["dt_bias"], pool,
+                              d["state_idx"], rings, torch.tensor(pos, device=DEV), torch.tensor(force, device=DEV),
+                              out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert rel_err(np64(o), o_ref[np.arange(B) * steps + t]) <= tol, t
+        pos = np.where((pos == L - 1) | (force != 0), 0, pos + 1).astype(np.int32)
+    assert kda.check_device_errors() == 0
+    used = inp["state_idx"].long()
+    assert rel_err(np64(pool)[used], p_ref[used]) <= tol
+
+
 @pytest.mark.parametrize("gate,io,L,D", [("kda", torch.bfloat16, 8, 128), ("kda", torch.float32, 16, 128),
                                           ("gdn", torch.bfloat16, 4, 128), ("kda", torch.float32, 8, 16),
                                           ("gdn", torch.bfloat16, 8, 32), ("kda", torch.float32, 5, 64),
