@@ -227,6 +227,14 @@ def barrier(dist):
 _PREFILL_HOST = {}
 
 
+def headline_config(T, world):
+    """The `config` of the headline line, the same for our arm and the reference arm."""
+    return {"workload": f"varlen_prefill_bf16: 8 seqs, lengths U[512,4096] (seed 1001), T={T}, H=32, d=128, "
+                        "chunk 64",
+            "io_dtype": "bf16", "out_dtype": "bf16", "state_dtype": "f32", "tokens_per_step": T,
+            "l2": "no flush: every working set > 129 MB L2", "parallelism": f"replicas x{world}"}
+
+
 def oracle_workload_once():
     """Oracle over the whole varlen workload (8 sequences, all 32 heads, threads over heads)."""
     import oracle
@@ -277,9 +285,7 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": f"varlen_prefill_bf16: 8 seqs, lengths U[512,4096] (seed 1001), T={T}, "
-                                   "H=32, d=128, chunk 64",
-                       "io_dtype": "bf16", "tokens_per_step": T},
+            "config": headline_config(T, world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
                              "sample": f"fp64 token recurrence over the whole varlen workload ({T} tokens, "
                                        f"8 sequences, 32 heads, threads over heads) per step"},
@@ -634,10 +640,7 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "varlen_prefill_bf16: 8 seqs, lengths U[512,4096] (seed 1001), "
-                               f"T={T}, H=32, d=128, chunk 64",
-                   "io_dtype": "bf16", "out_dtype": "bf16", "state_dtype": "f32", "tokens_per_step": T,
-                   "l2": "no flush: every working set > 129 MB L2", "parallelism": f"replicas x{world}"},
+        "config": headline_config(T, world),
         "roofline": roofline,
         **extra,
         "kernels": kernels,

@@ -1,6 +1,7 @@
 """The replica path of bench.py on two gloo ranks (CPU): rendezvous on 127.0.0.1, the barrier, and
 the max-over-ranks reduction that turns per-rank step times into the job's time.  The hot path
-has no exchange step, so these helpers are the whole multi-rank logic."""
+has no exchange step, so these helpers are the whole multi-rank logic.  Also the algorithmic byte
+counts and the reference arm's line (same metric, unit and config as our arm)."""
 import os
 import socket
 
@@ -78,3 +79,23 @@ def test_per_kernel_algorithmic_bytes_partition_the_call():
         assert bench.intra_bytes(T, H, D, io) + bench.state_pass_bytes(T, N, H, D, out) == call
     # per (token, head): q, k, v bf16 + g_raw fp32 + b_raw fp32 = 1284 bytes
     assert bench.intra_bytes(1, 1, 128, 2) - (4 + 128 * 4) == 1284
+
+
+def test_reference_arm_line_matches_our_arm(monkeypatch, capsys):
+    """The reference arm prints one line with our arm's metric, unit, direction and config, so that
+    the two lines compare like for like (the oracle's timing is stubbed: no compute here)."""
+    import argparse
+    import json
+
+    monkeypatch.setattr(bench, "oracle_workload_once", lambda: (0.5, 4, 16412))
+    monkeypatch.setattr(bench, "dist_env", lambda: (0, 1, 0))
+    import oracle
+    monkeypatch.setattr(oracle, "build", lambda *a, **k: None)
+    args = argparse.Namespace(gpus=1, steps=3, warmup=1)
+    assert bench.run_reference(args) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert (line["metric"], line["unit"], line["higher_is_better"]) == (bench.METRIC, bench.UNIT, True)
+    assert line["config"] == bench.headline_config(16412, 1)
+    assert line["value"] == pytest.approx(16412 / 0.5)
+    assert line["e2e"]["value"] == line["value"] and line["cpu_baseline"]["cores"] == 4
