@@ -1,6 +1,6 @@
-"""Numerics model of the bf16 tensor-core prefill (CPU only): the chunk algorithm evaluated in fp64
-with every operand rounded where the kernels round it, compared with the oracle's token
-recurrence on the same inputs.
+"""Numerics models (CPU only), evaluated in fp64 with every operand rounded where the kernels round
+it and compared with the oracle's token recurrence on the same inputs: the bf16 tensor-core
+prefill, and the ring of the buffered decode.
 
 Rounding points of the kernels (bf16 inputs, d = 128, chunk 64):
   * alpha, beta, k_hat, q_hat in fp32;
@@ -177,3 +177,62 @@ def test_bf16_operands_would_not(runs):
     e = max(_rel(o, o_ref), _rel(pl[used], p_ref[used]))
     print(f"bf16 operands: {e:.2e}")
     assert e > 2e-3, e
+
+
+def replay_model(inp, H, D, L, steps, B, ring_round):
+    """The buffered decode (ReplaySSM, sections 3.9-3.12) over `steps` tokens per request: each step
+    rebuilds S' from the checkpoint and the ring entries (d_j, k_hat_j, a_j) committed since, takes
+    the step, and either appends (d, k_hat, a) to the ring or, when the ring is full or at the last
+    step, writes the checkpoint.  `ring_round` rounds the stored d."""
+    q, k, v = (inp[n].double().numpy() for n in ("q", "k", "v"))
+    g_raw, b_raw = inp["g_raw"].double().numpy(), inp["b_raw"].double().numpy()
+    A_log, dtb = inp["A_log"].double().numpy(), inp["dt_bias"].double().numpy()
+    sidx = inp["state_idx"].numpy()
+    pool = inp["pool"].double().numpy().copy()
+    out = np.zeros((B * steps, H, D))
+    for b in range(B):
+        for h in range(H):
+            S0 = pool[sidx[b], h].T.copy()
+            ring = []
+            rate = math.exp(A_log[h])
+            for t in range(steps):
+                row = b * steps + t
+                x = g_raw[row, h] + dtb[h]
+                a = f32(np.exp(-rate * np.where(x > 20.0, x, np.log1p(np.exp(np.minimum(x, 20.0))))))
+                beta = f32(1.0 / (1.0 + np.exp(-b_raw[row, h])))
+                kk, qq = k[row, h], q[row, h]
+                kh = f32(kk / math.sqrt(kk @ kk + 1e-6))
+                qh = f32(qq / math.sqrt(qq @ qq + 1e-6) / math.sqrt(D))
+                Sr = S0.copy()
+                for d_j, k_j, a_j in ring:
+                    Sr = a_j[:, None] * Sr + np.outer(k_j, d_j)
+                Sd = a[:, None] * Sr
+                delta = beta * (v[row, h] - kh @ Sd)
+                S_t = Sd + np.outer(kh, delta)
+                out[row, h] = f32(qh @ S_t)
+                if len(ring) == L - 1 or t == steps - 1:
+                    S0, ring = f32(S_t), []
+                else:
+                    ring.append((ring_round(delta), kh, a))
+            pool[sidx[b], h] = S0.T
+    return out, pool
+
+
+def test_buffered_decode_ring_precision():
+    """Ring length 16, 6 requests x 4 heads, 33 steps: with fp32 ring entries the model matches the
+    oracle to rounding; with bf16 deltas (the state dtype some deployments choose) the error they
+    add alone is over a quarter of the 2e-3 bound, which is why the kernel keeps the ring in fp32."""
+    H, D, L, B, steps = 4, 128, 16, 6, 33
+    inp = workloads.make_inputs([steps] * B, H, D, torch.bfloat16, pool_slots=8, pool_std=0.05, seed=82,
+                                dt_bias_std=0.3)
+    p = oracle.make_params(H, D)
+    o_ref, p_ref, _ = oracle.forward(p, inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["b_raw"], inp["A_log"],
+                                     inp["dt_bias"], inp["cu_seqlens"], inp["pool"], inp["state_idx"])
+    used = inp["state_idx"].numpy()
+    errs = {}
+    for name, rnd in (("fp32", f32), ("bf16", bf16)):
+        o, pl = replay_model(inp, H, D, L, steps, B, rnd)
+        errs[name] = max(_rel(o, o_ref), _rel(pl[used], p_ref[used]))
+    print(f"buffered decode ring: fp32 {errs['fp32']:.2e}, bf16 {errs['bf16']:.2e}")
+    assert errs["fp32"] <= 1e-5
+    assert errs["bf16"] > 5e-4
