@@ -29,6 +29,9 @@
  *                 non-negative entries must be distinct.  An entry >= num_slots is treated as
  *                 padding and recorded as a device error (kda_check_device_errors).
  *   - D = d_k = d_v = head_dim.
+ *   - q, k, v, g_raw, dt_bias (when given), state_pool, out and the intermediate-state, snapshot
+ *     and ring buffers must be 16-byte aligned (KDA_ERR_MISALIGNED otherwise); b_raw, A_log,
+ *     cu_seqlens, state_idx and the other int32 tables need only their element alignment.
  *   - All host-side checks (NULL pointers, sizes, alignment, supported shapes) run before any
  *     work is enqueued and return a status without touching memory.  Work is then enqueued on
  *     `stream` and the call returns without synchronising; a launch failure is reported as
@@ -105,7 +108,8 @@ const char* kda_status_string(int32_t status);
  *   cu_seqlens    device int32 [num_seqs + 1], non-decreasing, cu_seqlens[0] = 0,
  *                 cu_seqlens[num_seqs] = total_tokens.  Never read back to the host; a malformed
  *                 table is clamped and recorded as a device error.
- *   total_tokens  T >= 0 (the number of rows of q, k, v, g_raw, b_raw, out).
+ *   total_tokens  0 <= T < 2^31 - 64 (the number of rows of q, k, v, g_raw, b_raw, out); a
+ *                 larger T returns KDA_ERR_UNSUPPORTED.
  *   workspace     device scratch of at least kda_chunk_prefill_workspace_size(...) bytes,
  *                 256-byte aligned, owned by the caller; its contents need not be initialised
  *                 and are garbage afterwards.  It must not be shared with a call that overlaps
