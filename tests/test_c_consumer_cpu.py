@@ -1,18 +1,22 @@
 """The C ABI from plain C (no GPU needed): a C99 program that includes include/kda.h compiles with
 -std=c99 -pedantic -Wall -Wextra -Werror, links against libkda.so, and its host-side calls return
 the documented results: the defaults, the status strings, the workspace size, and the argument
-checks that return before any work is enqueued (no pointer passed is ever dereferenced)."""
+checks that return before any work is enqueued (no pointer passed is ever dereferenced).  The
+program also reports the layout of kda_params, which the Python binding's ctypes mirror must
+match field by field."""
+import ctypes
 import os
 import shutil
 import subprocess
 
 import pytest
 
-from kda_gated_delta_gb300 import build
+from kda_gated_delta_gb300 import binding, build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 PROGRAM = r"""
+#include <stddef.h>
 #include <stdio.h>
 #include <string.h>
 #include "kda.h"
@@ -54,6 +58,14 @@ int main(void)
     rc = kda_recurrent_verify(&p, dev, dev, dev, f, f, f, NULL, 4, 17, f, 8, idx, f, dev, NULL);
     EXPECT(rc == KDA_ERR_INVALID_ARG, 10);
 
+    /* the struct layout, for the comparison with the Python binding's mirror */
+    printf("layout %zu", sizeof(kda_params));
+    printf(" num_heads=%zu head_dim=%zu io_dtype=%zu out_dtype=%zu gate_kind=%zu chunk_size=%zu",
+           offsetof(kda_params, num_heads), offsetof(kda_params, head_dim), offsetof(kda_params, io_dtype),
+           offsetof(kda_params, out_dtype), offsetof(kda_params, gate_kind), offsetof(kda_params, chunk_size));
+    printf(" use_lower_bound=%zu lower_bound=%zu scale=%zu l2_eps=%zu softplus_threshold=%zu\n",
+           offsetof(kda_params, use_lower_bound), offsetof(kda_params, lower_bound), offsetof(kda_params, scale),
+           offsetof(kda_params, l2_eps), offsetof(kda_params, softplus_threshold));
     printf("ok %zu\n", ws);
     return 0;
 }
@@ -78,4 +90,12 @@ def test_c99_program_compiles_links_and_runs(tmp_path, lib_dir):
     assert r.returncode == 0, r.stderr
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
-    assert r.stdout.startswith("ok ")
+    lines = r.stdout.strip().splitlines()
+    assert lines[-1].startswith("ok ")
+    # the binding's ctypes mirror of kda_params has the C compiler's size and field offsets
+    layout = lines[-2].split()
+    assert layout[0] == "layout" and int(layout[1]) == ctypes.sizeof(binding.Params)
+    for item in layout[2:]:
+        name, off = item.split("=")
+        assert getattr(binding.Params, name).offset == int(off), name
+    assert len(layout) - 2 == len(binding.Params._fields_)
