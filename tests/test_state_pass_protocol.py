@@ -316,3 +316,43 @@ def test_wrong_drain_phase_is_caught(wrong):
             except AssertionError:
                 failures += 1
     assert failures > 0
+
+
+def _kernel_barriers():
+    """Barrier name -> arrival count per slot, read from chunk_state_tc_kernel's initialisation."""
+    import os
+    import re
+    src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "kda_gated_delta_gb300", "csrc", "kda_prefill.cu")).read()
+    body = src[src.index("chunk_state_tc_kernel(const StateArgs a)"):]
+    block = body[:body.index("tc::fence_mbar_init();")]
+    block = block[block.rindex("if (tid == 0) {"):]
+    bars = {}
+    # statements, with "for (int i = 0; i < N; ++i) { ... }" or a single statement after it expanded
+    for m in re.finditer(r"for \(int i = 0; i < (\d+); \+\+i\) (\{[^}]*\}|[^;]*;)", block):
+        n = int(m.group(1))
+        for name, count in re.findall(r"mbar_init\(&bars->(\w+)\[i\], (\d+)\)", m.group(2)):
+            bars[name] = [int(count)] * n
+    rest = re.sub(r"for \(int i = 0; i < \d+; \+\+i\) (\{[^}]*\}|[^;]*;)", "", block)
+    for name, idx, count in re.findall(r"mbar_init\(&bars->(\w+)(?:\[(\d+)\])?, (\d+)\)", rest):
+        if idx:
+            slots = bars.setdefault(name, [])
+            assert int(idx) == len(slots), (name, idx)
+            slots.append(int(count))
+        else:
+            bars[name] = int(count)
+    return bars
+
+
+def test_model_mirrors_the_kernel_barriers():
+    """The model's barriers have the kernel's ring depths and arrival counts (the issuers' drain
+    barriers, used once after the loop, are not part of the chunk protocol)."""
+    k = _kernel_barriers()
+    M = Model(1, 0)
+    names = {"w": "w", "kt": "kt", "u": "u", "qp": "qp", "o": "o", "delta_ready": "delta", "sh_ready": "sh",
+             "zw_ready": "zw", "chain": "chain", "c": "c", "z": "z", "dz_free": "dz_free", "do_free": "do_free"}
+    assert set(k) - {"drain"} == set(names), sorted(k)
+    for kname, mname in names.items():
+        mb = getattr(M, mname)
+        got = [b.count for b in mb] if isinstance(mb, list) else mb.count
+        assert got == k[kname], (kname, got, k[kname])
