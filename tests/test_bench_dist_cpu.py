@@ -69,6 +69,18 @@ def test_algorithmic_byte_counts():
     assert bench.verify_bytes(1, 4, 1, 128, 2, 2) == 65536 + 4 * (65536 + 768 + 4 + 4 + 256) + 8
 
 
+def test_buffered_decode_bytes_follow_the_halving_model():
+    """ReplaySSM, section 12: the plain decode reads and writes the whole fp32 state every step; the
+    buffered decode reads the checkpoint every step and writes it once per ring of L steps, so with
+    staggered cursors its state traffic per step is (1 + 1/L) / 2 of the plain decode's.  The vector
+    terms (token inputs, ring entries) fade against it as d grows."""
+    for L in (8, 16):
+        cursors = list(range(L))                 # one request in L flushes at each step
+        for D, tol in ((128, 0.15), (4096, 0.01)):
+            ratio = bench.replay_bytes(cursors, L, 1, D, 2, 2) / bench.decode_bytes(L, 1, D, 2, 2)
+            assert abs(ratio - (1 + 1 / L) / 2) < tol, (L, D, ratio)
+
+
 def test_per_kernel_algorithmic_bytes_partition_the_call():
     """The intra kernel's bytes (token inputs once) and the state pass's (states read and written,
     output written) add up to the prefill call's algorithmic bytes: the dominant-kernel roofline
