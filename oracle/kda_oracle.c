@@ -18,8 +18,10 @@
  * Pins: every function here is checked by tests that do not call this file's formulas again
  * (tests/test_oracle_pins.py): the overwrite property, orthonormal readback, the prefix-sum
  * special case, the gradient-step identity, the beta-interpolation identity, contraction with
- * v = 0, the GDN-inside-KDA special case, the printed safe-gate half-lives and agreement of the
- * chunk closed form with the token recurrence.
+ * v = 0, the GDN-inside-KDA special case, the printed safe-gate half-lives, the explicit q scale,
+ * the argument checks and agreement of the chunk closed form with the token recurrence.  A
+ * mutation test (tests/test_oracle_mutants.py) plants one-line mistakes in copies of this file
+ * and checks that the pins catch each of them.
  */
 #include <math.h>
 #include <stdint.h>
