@@ -124,6 +124,7 @@ def test_prefill_validation_and_workspace(L):
     assert call(p, cu=None) == -1
     assert call(p, T=0) == 0 and call(p, N=0) == 0
     assert call(p, N=-1) == -1
+    assert call(p, T=(1 << 31) - 64, ws_bytes=1 << 40) == -2    # total_tokens limit (kda.h)
 
 
 def test_selftest_validation(L):
