@@ -9,7 +9,6 @@
 The oracle runs on a small pool (the used slots renumbered 0..n-1) and, for the long call, on a
 subset of heads sliced out of the inputs; heads are independent in the recurrence, so both are
 exact restatements of the same computation."""
-import numpy as np
 import pytest
 import torch
 
