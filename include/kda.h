@@ -262,16 +262,17 @@ int32_t kda_commit_verified_states(const kda_params* p,
  * KDA_STATIC_SCRATCH_BYTES compiled into the library.  A device holds that much memory for it
  * until its context is destroyed (normally at process exit): under CUDA's default lazy module
  * loading from the first call of this entry point on that device, under eager loading
- * (CUDA_MODULE_LOADING=EAGER) from the creation of the context.  The call allocates nothing.  A problem whose kda_chunk_prefill_workspace_size(...) exceeds
- * KDA_STATIC_SCRATCH_BYTES is rejected with KDA_ERR_SCRATCH_LIMIT before any work is enqueued
+ * (CUDA_MODULE_LOADING=EAGER) from the creation of the context.  The call allocates nothing.
+ * A problem whose kda_chunk_prefill_workspace_size(...) exceeds KDA_STATIC_SCRATCH_BYTES is
+ * rejected with KDA_ERR_SCRATCH_LIMIT before any work is enqueued
  * (with bf16 inputs, H = 32, head_dim = 128, chunk 64 the array covers ceil(T / 64) + num_seqs
  * <= 112 chunks, about 7,000 tokens per call).
  *
  * Every call looks up the device address of the array in the current context (nothing is
  * cached, so a context that was reset and created again is handled); under lazy loading the
  * first call on a device also loads the library's device code there, so make that first call
- * outside any stream capture.  All calls share the one array and it keeps whatever the last call left in it (nothing in it
- * needs to start at zero).  Calls whose kernels overlap on the GPU, on different streams or
+ * outside any stream capture.  All calls share the one array and it keeps whatever the last
+ * call left in it (nothing in it needs to start at zero).  Calls whose kernels overlap on the GPU, on different streams or
  * from different host threads, race on the array and produce garbage: order them.
  */
 #define KDA_STATIC_SCRATCH_BYTES ((size_t)256 << 20)
