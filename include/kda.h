@@ -272,8 +272,9 @@ int32_t kda_commit_verified_states(const kda_params* p,
  * cached, so a context that was reset and created again is handled); under lazy loading the
  * first call on a device also loads the library's device code there, so make that first call
  * outside any stream capture.  All calls share the one array and it keeps whatever the last
- * call left in it (nothing in it needs to start at zero).  Calls whose kernels overlap on the GPU, on different streams or
- * from different host threads, race on the array and produce garbage: order them.
+ * call left in it (nothing in it needs to start at zero).  Calls whose kernels overlap on the
+ * GPU, on different streams or from different host threads, race on the array and produce
+ * garbage: order them.
  */
 #define KDA_STATIC_SCRATCH_BYTES ((size_t)256 << 20)
 int32_t kda_chunk_prefill_static_scratch(const kda_params* p,
